@@ -1,0 +1,94 @@
+// Host-side declarations shared by the fp4moe translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp4moe {
+
+constexpr int kTokPerBlk = 32;   // tokens per routing / scatter block
+constexpr int kMaxE = 1024;      // experts supported by the routing kernels
+constexpr int kMaxTopK = 16;
+constexpr int kTileN = 128;      // packed weight tile rows (UMMA M)
+constexpr int kTileK = 64;       // packed weight tile K (one 128-B bf16 row)
+constexpr int kTileDataBytes = kTileN * kTileK / 2;  // 4096
+
+// Packed tile bytes for a scale granularity: E2M1 data + one scale code per
+// group and row.
+constexpr int tile_bytes(int gran) {
+  return kTileDataBytes + kTileN * (kTileK / gran);
+}
+
+// ---------------------------------------------------------------- kernels
+cudaError_t launch_requant(const uint8_t* fp4, const uint8_t* s16,
+                           int64_t rows, int64_t K, uint8_t* fp4_out,
+                           uint8_t* s32_out, int* err, cudaStream_t st);
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t T, int64_t K,
+                             uint8_t* xq, uint8_t* xs, int* err,
+                             cudaStream_t st);
+
+// FP8 rounding of FP32 h [rows, I] to exact-bf16 E4M3 x UE8M0/32 values.
+cudaError_t launch_h_fp8_round(const float* h, int64_t rows, int64_t I,
+                               uint16_t* out, cudaStream_t st);
+
+// S2: ids/w per pair and a per-block expert histogram hist[nblk][E].
+cudaError_t launch_route(const float* logits, int T, int E, int k,
+                         int32_t* ids, float* w, int32_t* hist, int* err,
+                         cudaStream_t st);
+
+// S3 (scan): counts, offsets, per-block bases, and the GEMM token-chunk
+// prefix cstart[E+1] for chunks of at most chunk_max tokens.
+cudaError_t launch_scan(int T, int E, const int32_t* hist, int32_t* base,
+                        int32_t* counts, int32_t* offsets, int32_t* cstart,
+                        int chunk_max, cudaStream_t st);
+
+// S3 (scatter): perm/inv and, if xperm != nullptr, the gathered activation
+// rows in expert-major order as bf16 (FP8 inputs are dequantized exactly).
+cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
+                           const int32_t* base, int32_t* perm, int32_t* inv,
+                           const void* x, const uint8_t* xs, int K,
+                           int act_mode, uint16_t* xperm, cudaStream_t st);
+
+// S7: y[t] = sum_j w[t,j] * o[inv[t,j]] -> bf16.
+cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
+                           int T, int k, int K, uint16_t* y, cudaStream_t st);
+
+// S0: pack one weight matrix [E, N, Kd] into tiles.  gated: FC1 gate/up
+// interleave with `layout` giving the source half order.  bmax: per-expert
+// maximum UE8M0 byte (gran 32) or nullptr.
+cudaError_t launch_scale_max(const uint8_t* s, int E, int64_t per_expert,
+                             int32_t* bmax, int* err, cudaStream_t st);
+cudaError_t launch_pack(const uint8_t* w, const uint8_t* s, int E, int N,
+                        int Kd, int gran, bool gated, int layout,
+                        const int32_t* bmax, uint8_t* out, int* err,
+                        cudaStream_t st);
+cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E,
+                         int gran, float* alpha, cudaStream_t st);
+
+// S5 / S6: grouped GEMM over packed weights.
+struct GemmArgs {
+  const uint8_t* wpack;    // packed tiles [E][N/128][Kd/64]
+  const float* alpha;      // [E] epilogue scale
+  const int32_t* offsets;  // [E+1] token offsets (expert-major rows)
+  const int32_t* cstart;   // [E+1] token-chunk prefix
+  void* out;               // FC1: h [P, N/2]; FC2: o f32 [P, N]
+  int* err;
+  int E, nblocks, ksteps, tile_bytes, gran;
+  uint32_t smul, sadd;     // scale code -> bf16 bits
+  int ldo;                 // output row stride in elements
+  int mode;                // 0: FC1 + SwiGLU (bf16 h), 1: FC2 (f32 o),
+                           // 2: FC1 + SwiGLU writing FP32 h (rounded to
+                           //    E4M3 x UE8M0/32 by launch_h_fp8_round)
+};
+constexpr int kGemmModeFc1 = 0, kGemmModeFc2 = 1, kGemmModeFc1Fp8 = 2;
+
+cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
+                        int num_sms, cudaStream_t st);
+
+// Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
+int gemm_chunk_max(int T);
+
+}  // namespace fp4moe

@@ -1,0 +1,712 @@
+// Memory-bound kernels of the block-scaled FP4 MoE path (sm_103a): the
+// group16 -> group32 requant, FP8 activation quantization, routing, the
+// expert-major permutation and activation gather, the weighted combine, and
+// the weight packing of prepare_weights.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+int g_num_sms = 0;
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 1;
+  }
+  return g_num_sms;
+}
+
+// ================================================================ requant
+//
+// group16 -> group32 requant ("glm52_nvfp4_group16_notes.md", section
+// "Requantization path").  One thread owns one 32-element group: 16 bytes of
+// codes and two E4M3 scales in, 16 bytes of codes and one UE8M0 byte out.
+// Because the scale of a half is constant, the new code of each element
+// depends only on its half, its 3-bit magnitude and its sign.  The thread
+// builds, per half, an 8-entry table new_mag[m] = RNE(e2m1(m) * |s| / 2^e)
+// with the hardware E2M1 conversion, maps all 32 nibbles through it with byte
+// permutes, and passes the sign through (flipped for a negative scale).
+
+// E2M1 magnitude of a 3-bit code, exactly: placing (e1 e0 m) at float bits
+// 24..22 gives e2m1 * 2^-126, including the subnormal code 1 (0.5).
+__device__ __forceinline__ float e2m1_mag(uint32_t m) {
+  return __uint_as_float(m << 22) * 0x1p126f;
+}
+
+// Largest 3-bit magnitude among the 16 nibbles of two words.
+__device__ __forceinline__ uint32_t max_mag16(uint32_t a, uint32_t b) {
+  uint32_t x = __vmaxu4(a & 0x07070707u, (a >> 4) & 0x07070707u);
+  uint32_t y = __vmaxu4(b & 0x07070707u, (b >> 4) & 0x07070707u);
+  uint32_t m = __vmaxu4(x, y);
+  m = __vmaxu4(m, m >> 16);
+  m = __vmaxu4(m, m >> 8);
+  return m & 0xFFu;
+}
+
+// Table of new magnitudes for f = |s| / 2^e: byte m of (lo, hi) = new mag m.
+__device__ __forceinline__ void build_lut(float f, uint32_t& lo, uint32_t& hi) {
+  const uint32_t c01 = f32x2_to_e2m1x2(0.0f, 0.5f * f);
+  const uint32_t c23 = f32x2_to_e2m1x2(1.0f * f, 1.5f * f);
+  const uint32_t c45 = f32x2_to_e2m1x2(2.0f * f, 3.0f * f);
+  const uint32_t c67 = f32x2_to_e2m1x2(4.0f * f, 6.0f * f);
+  lo = (c01 & 0x7u) | ((c01 & 0x70u) << 4) | ((c23 & 0x7u) << 16) |
+       ((c23 & 0x70u) << 20);
+  hi = (c45 & 0x7u) | ((c45 & 0x70u) << 4) | ((c67 & 0x7u) << 16) |
+       ((c67 & 0x70u) << 20);
+}
+
+// Maps the 8 nibbles of w through the table; sign bits pass through XOR sx.
+__device__ __forceinline__ uint32_t remap8(uint32_t w, uint32_t lo, uint32_t hi,
+                                           uint32_t sx) {
+  const uint32_t r0 = __byte_perm(lo, hi, w & 0x7777u);
+  const uint32_t r1 = __byte_perm(lo, hi, (w >> 16) & 0x7777u);
+  const uint32_t t0 = r0 | (r0 >> 4);
+  const uint32_t t1 = r1 | (r1 >> 4);
+  return __byte_perm(t0, t1, 0x6420) | ((w & 0x88888888u) ^ sx);
+}
+
+__global__ void __launch_bounds__(256) requant_kernel(
+    const uint8_t* __restrict__ fp4, const uint8_t* __restrict__ s16,
+    int64_t groups, uint8_t* __restrict__ out, uint8_t* __restrict__ s32,
+    int* err) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g < groups; g += stride) {
+    const uint4 d = __ldcs(reinterpret_cast<const uint4*>(fp4) + g);
+    const uint32_t sc = __ldcs(reinterpret_cast<const uint16_t*>(s16) + g);
+    const uint32_t sb0 = sc & 0xFFu, sb1 = sc >> 8;
+    uint4 o;
+    uint32_t byte;
+    if ((sb0 & 0x7Fu) == 0x7Fu || (sb1 & 0x7Fu) == 0x7Fu) {
+      record_error(err, FP4MOE_ERR_INVALID_ARG);
+      o = make_uint4(0, 0, 0, 0);
+      byte = 0xFFu;
+    } else {
+      const float2 s = e4m3x2_to_f32x2(sc);
+      const float a0 = fabsf(s.x), a1 = fabsf(s.y);
+      const float amax = fmaxf(e2m1_mag(max_mag16(d.x, d.y)) * a0,
+                               e2m1_mag(max_mag16(d.z, d.w)) * a1);
+      int e = 0;
+      if (amax > 0.0f) {
+        // amax = 1.f * 2^E; 6 * 2^(E-2) = 1.5 * 2^E covers f <= 1.5.
+        const uint32_t bits = __float_as_uint(amax);
+        const int E = static_cast<int>(bits >> 23) - 127;
+        e = ((bits & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;
+      }
+      e = max(-127, min(127, e));
+      byte = static_cast<uint32_t>(e + 127);
+      // |s| / 2^e: e is in [-13, 9] for any finite non-zero group, so the
+      // power of two is a normal float.
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      uint32_t l0, h0, l1, h1;
+      build_lut(a0 * inv, l0, h0);
+      build_lut(a1 * inv, l1, h1);
+      const uint32_t sx0 = (sb0 & 0x80u) ? 0x88888888u : 0u;
+      const uint32_t sx1 = (sb1 & 0x80u) ? 0x88888888u : 0u;
+      o.x = remap8(d.x, l0, h0, sx0);
+      o.y = remap8(d.y, l0, h0, sx0);
+      o.z = remap8(d.z, l1, h1, sx1);
+      o.w = remap8(d.w, l1, h1, sx1);
+    }
+    __stcs(reinterpret_cast<uint4*>(out) + g, o);
+    s32[g] = static_cast<uint8_t>(byte);
+  }
+}
+
+// ============================================================== act quant
+//
+// Recipe (1,1,32) of the group16 notes page: per token and 32 consecutive K
+// elements, UE8M0 e = min{e : amax <= 448 * 2^e}, q = E4M3(x / 2^e).
+
+__device__ __forceinline__ uint32_t ue8m0_for_e4m3(float amax) {
+  if (!(amax > 0.0f)) return 127u;
+  const uint32_t bits = __float_as_uint(amax);
+  const int field = static_cast<int>(bits >> 23);
+  if (field == 0) return 0u;  // below 2^-126: the clamp gives byte 0
+  const int E = field - 127;
+  // 448 = 1.75 * 2^8: 448 * 2^(E-8) covers mantissas up to 1.75.
+  const int e = ((bits & 0x7FFFFFu) <= 0x600000u) ? E - 8 : E - 7;
+  return static_cast<uint32_t>(max(0, min(254, e + 127)));
+}
+
+__global__ void __launch_bounds__(256) act_quant_kernel(
+    const uint16_t* __restrict__ x, int64_t groups, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int* err) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g < groups; g += stride) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + g * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = src[i];
+      w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    if (!(amax <= 3.402823466e38f)) {  // inf or NaN
+      record_error(err, FP4MOE_ERR_INVALID_ARG);
+      amax = 0.0f;
+    }
+    const uint32_t byte = ue8m0_for_e4m3(amax);
+    const int e = static_cast<int>(byte) - 127;   // <= 120 for bf16 inputs
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * i]) * inv,
+                                          bf16_hi(w[2 * i]) * inv);
+      const uint32_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * i + 1]) * inv,
+                                          bf16_hi(w[2 * i + 1]) * inv);
+      o[i] = lo | (hi << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + g * 32);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    s[g] = static_cast<uint8_t>(byte);
+  }
+}
+
+// FP8 rounding of the FC1 output h (FP8 activation path): per row and 32
+// consecutive columns, the same UE8M0 + E4M3 rule as the activation
+// quantization, stored back as the exact bf16 value q * 2^e for FC2.
+__device__ __forceinline__ float pow2_any(int e) {  // 2^e, e in [-149, 127]
+  return (e >= -126) ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                     : __uint_as_float(1u << (e + 149));
+}
+
+__global__ void __launch_bounds__(256) h_fp8_round_kernel(
+    const float* __restrict__ h, int64_t groups, uint16_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g < groups; g += stride) {
+    const float4* src = reinterpret_cast<const float4*>(h + g * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 t = src[i];
+      v[4 * i] = t.x, v[4 * i + 1] = t.y, v[4 * i + 2] = t.z, v[4 * i + 3] = t.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = static_cast<int>(ue8m0_for_e4m3(amax)) - 127;
+    const float inv = pow2_any(-e), sc = pow2_any(e);
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 q = e4m3x2_to_f32x2(f32x2_to_e4m3x2(v[2 * i] * inv, v[2 * i + 1] * inv));
+      o[i] = pack_bf16x2(q.x * sc, q.y * sc);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + g * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  }
+}
+
+// ================================================================ routing
+//
+// Softmax top-k with renormalised weights.  One warp per token; each lane
+// holds EPL logits (expert lane + 32 i).  k rounds of a warp arg-max
+// (larger value wins, equal values go to the lower expert id) select the
+// experts on the raw logits; w_j = exp(l_j - l_0) / sum over the k.
+
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_kernel(
+    const float* __restrict__ logits, int T, int E, int k,
+    int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ hist, int* err) {
+  __shared__ int cnt[kMaxE];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTokPerBlk + warp;
+  if (t < T && warp < kTokPerBlk) {
+    float v[EPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        v[i] = logits[static_cast<int64_t>(t) * E + e];
+        if (v[i] != v[i]) {
+          record_error(err, FP4MOE_ERR_INVALID_ARG);
+          v[i] = -INFINITY;
+        }
+      } else {
+        v[i] = -INFINITY;
+        taken |= 1u << i;
+      }
+    }
+    float my_v = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oi = __shfl_xor_sync(kFull, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_id = bi;
+      }
+    }
+    const float v0 = __shfl_sync(kFull, my_v, 0);
+    const float ex = (lane < k) ? expf(my_v - v0) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+      ids[static_cast<int64_t>(t) * k + lane] = my_id;
+      w[static_cast<int64_t>(t) * k + lane] = ex / sum;
+      atomicAdd(&cnt[my_id], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// Exclusive block scan over blockDim.x (== 1024) values; returns the
+// exclusive prefix and writes the total to *total.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, s, off);
+      if (lane >= off) s += y;
+    }
+    wsum[lane] = s;
+  }
+  __syncthreads();
+  const int incl = x + (warp > 0 ? wsum[warp - 1] : 0);
+  *total = wsum[31];
+  __syncthreads();
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(
+    int nblk, int E, const int32_t* __restrict__ hist, int32_t* __restrict__ base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ cstart, int chunk_max) {
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) tot += hist[static_cast<int64_t>(b) * E + e];
+  int total;
+  const int off = block_exclusive_scan(e < E ? tot : 0, &total);
+  const int nch = (e < E) ? (tot + chunk_max - 1) / chunk_max : 0;
+  int ctotal;
+  const int coff = block_exclusive_scan(nch, &ctotal);
+  if (e < E) {
+    counts[e] = tot;
+    offsets[e] = off;
+    cstart[e] = coff;
+    int run = off;
+    for (int b = 0; b < nblk; ++b) {
+      const int64_t i = static_cast<int64_t>(b) * E + e;
+      const int c = hist[i];
+      base[i] = run;
+      run += c;
+    }
+  }
+  if (e == 0) {
+    offsets[E] = total;
+    cstart[E] = ctotal;
+  }
+}
+
+// Stable scatter: within block b (tokens [32b, 32b+32)), the rank of pair p
+// among the block's pairs of the same expert is the number of lower-indexed
+// pairs of that expert: earlier warps (per-warp counts in shared memory) plus
+// lower lanes of this warp (match mask).  Then the block copies each pair's
+// activation row into its expert-major slot.
+__global__ void __launch_bounds__(512) scatter_kernel(
+    const int32_t* __restrict__ ids, int T, int E, int k,
+    const int32_t* __restrict__ base, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, const void* __restrict__ x,
+    const uint8_t* __restrict__ xs, int K, int act_mode,
+    uint16_t* __restrict__ xperm) {
+  extern __shared__ int wcnt[];   // [16 warps][E]
+  __shared__ int spos[kTokPerBlk * kMaxTopK];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t P = static_cast<int64_t>(T) * k;
+  const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kTokPerBlk * k;
+  const int np = static_cast<int>(min(P - p0, static_cast<int64_t>(kTokPerBlk) * k));
+  for (int i = tid; i < 16 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const bool act = tid < np;
+  const int e = act ? ids[p0 + tid] : -1;
+  const unsigned m = __match_any_sync(kFull, e);
+  const int rank = __popc(m & ((1u << lane) - 1u));
+  if (act && rank == 0) wcnt[warp * E + e] = __popc(m);
+  __syncthreads();
+  if (act) {
+    int pre = 0;
+    for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E + e];
+    const int pos = base[static_cast<int64_t>(blockIdx.x) * E + e] + pre + rank;
+    perm[pos] = static_cast<int32_t>(p0 + tid);
+    inv[p0 + tid] = pos;
+    spos[tid] = pos;
+  }
+  if (xperm == nullptr) return;
+  __syncthreads();
+  for (int i = warp; i < np; i += 16) {
+    const int64_t t = (p0 + i) / k;
+    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<int64_t>(spos[i]) * K);
+    if (act_mode == FP4MOE_ACT_BF16) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint16_t*>(x) + t * K);
+      for (int c = lane; c < K / 8; c += 32) dst[c] = src[c];
+    } else {
+      // FP8: bf16(e4m3 * 2^(xs - 127)), exact for scaled values in the
+      // bf16 normal range.
+      const uint2* src = reinterpret_cast<const uint2*>(
+          static_cast<const uint8_t*>(x) + t * K);
+      const uint8_t* srow = xs + t * (K / 32);
+      for (int c = lane; c < K / 8; c += 32) {
+        const uint2 q = src[c];
+        const uint32_t sb = srow[c / 4];
+        const float sc = (sb == 0)     ? __uint_as_float(0x00400000u)
+                         : (sb == 255) ? __uint_as_float(0x7FC00000u)
+                                       : __uint_as_float(sb << 23);
+        const float2 a = e4m3x2_to_f32x2(q.x), b = e4m3x2_to_f32x2(q.x >> 16);
+        const float2 c2 = e4m3x2_to_f32x2(q.y), d2 = e4m3x2_to_f32x2(q.y >> 16);
+        dst[c] = make_uint4(pack_bf16x2(a.x * sc, a.y * sc),
+                            pack_bf16x2(b.x * sc, b.y * sc),
+                            pack_bf16x2(c2.x * sc, c2.y * sc),
+                            pack_bf16x2(d2.x * sc, d2.y * sc));
+      }
+    }
+  }
+}
+
+// ================================================================ combine
+
+__global__ void __launch_bounds__(256) combine_kernel(
+    const float* __restrict__ o, const int32_t* __restrict__ inv,
+    const float* __restrict__ w, int k, int K, uint16_t* __restrict__ y) {
+  const int64_t t = blockIdx.x;
+  int pos[kMaxTopK];
+  float wt[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      pos[j] = inv[t * k + j];
+      wt[j] = w[t * k + j];
+    }
+  }
+  for (int n = threadIdx.x * 8; n < K; n += blockDim.x * 8) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const float4* row =
+            reinterpret_cast<const float4*>(o + static_cast<int64_t>(pos[j]) * K + n);
+        const float4 a = row[0], b = row[1];
+        acc[0] = fmaf(wt[j], a.x, acc[0]);
+        acc[1] = fmaf(wt[j], a.y, acc[1]);
+        acc[2] = fmaf(wt[j], a.z, acc[2]);
+        acc[3] = fmaf(wt[j], a.w, acc[3]);
+        acc[4] = fmaf(wt[j], b.x, acc[4]);
+        acc[5] = fmaf(wt[j], b.y, acc[5]);
+        acc[6] = fmaf(wt[j], b.z, acc[6]);
+        acc[7] = fmaf(wt[j], b.w, acc[7]);
+      }
+    }
+    *reinterpret_cast<uint4*>(y + t * K + n) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// ================================================================ prepare
+//
+// Packed tile (e, nb, ks): 128 weight rows x 64 K elements, contiguous:
+//   [0, 4096)      E2M1 data: [2 halves of 32 K][128 rows][16 bytes]; each
+//                  16-byte row half is 4 words of 8 elements whose bits are
+//                  placed so that the GEMM's dequantizer needs only rotates
+//                  and masks (see dequant8 in gemm.cu);
+//   [4096, ...)    scale codes: [128 rows][64 / gran bytes].
+// FC1 tiles interleave gate and up rows: in row r = 32 q + l, l < 16 is gate
+// row i = 64 nb + 16 q + l and l >= 16 is up row i = 64 nb + 16 q + (l - 16).
+// Scale codes: gran 16 -> c with bf16(s * 2^119) = c * 16 + 0x7680 (the E4M3
+// exponent renormalised so subnormal scales are exact; a negative scale
+// flips the codes' signs; a zero scale zeroes the codes); gran 32 ->
+// c = b - bmax + 254 with bf16 bits c * 128 (scales more than 2^126 below the
+// matrix maximum flush to zero).
+
+// Bit positions of element j (k offset 0..7) in a packed word: the 3
+// magnitude bits start at kMagPos[j], the sign bit sits at kSgnPos[j].
+__constant__ uint8_t kMagPos[8] = {6, 22, 3, 19, 0, 16, 27, 11};
+__constant__ uint8_t kSgnPos[8] = {15, 31, 14, 30, 9, 25, 10, 26};
+
+__device__ __forceinline__ uint32_t pack8(const uint8_t* c) {
+  uint32_t x = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    x |= (static_cast<uint32_t>(c[j] & 7u) << kMagPos[j]) |
+         (static_cast<uint32_t>((c[j] >> 3) & 1u) << kSgnPos[j]);
+  return x;
+}
+
+__global__ void scale_max_kernel(const uint8_t* __restrict__ s,
+                                 int64_t per_expert, int32_t* bmax, int* err) {
+  const int e = blockIdx.y;
+  const uint8_t* p = s + static_cast<int64_t>(e) * per_expert;
+  int m = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < per_expert; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = p[i];
+    if (b == 255)
+      record_error(err, FP4MOE_ERR_INVALID_ARG);
+    else
+      m = max(m, b);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(bmax + e, m);
+}
+
+__global__ void __launch_bounds__(128) pack_kernel(
+    const uint8_t* __restrict__ w, const uint8_t* __restrict__ s, int E, int N,
+    int Kd, int gran, int gated, int layout, const int32_t* __restrict__ bmax,
+    uint8_t* __restrict__ out, int* err) {
+  const int nblocks = N / kTileN, ksteps = Kd / kTileK;
+  const int64_t tile = blockIdx.x;
+  const int r = threadIdx.x;
+  const int ks = static_cast<int>(tile % ksteps);
+  const int64_t t2 = tile / ksteps;
+  const int nb = static_cast<int>(t2 % nblocks);
+  const int e = static_cast<int>(t2 / nblocks);
+  int src;
+  if (gated) {
+    const int I = N / 2, q = r >> 5, l = r & 31;
+    const int i = 64 * nb + 16 * q + (l & 15);
+    const int gate0 = (layout == FP4MOE_W13_GATE_UP) ? 0 : I;
+    const int up0 = (layout == FP4MOE_W13_GATE_UP) ? I : 0;
+    src = ((l < 16) ? gate0 : up0) + i;
+  } else {
+    src = kTileN * nb + r;
+  }
+  const int64_t row = static_cast<int64_t>(e) * N + src;
+  const uint4* wsrc =
+      reinterpret_cast<const uint4*>(w + row * (Kd / 2) + ks * (kTileK / 2));
+  const uint4 b0 = wsrc[0], b1 = wsrc[1];
+  const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  uint8_t codes[64];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) codes[8 * i + j] = (bw[i] >> (4 * j)) & 0xFu;
+  const int ng = kTileK / gran;
+  const uint8_t* srow = s + row * (Kd / gran) + ks * ng;
+  uint8_t* tp = out + tile * tile_bytes(gran);
+  for (int g = 0; g < ng; ++g) {
+    const uint32_t sb = srow[g];
+    uint32_t code = 0;
+    bool zero = false, neg = false;
+    if (gran == 16) {
+      const uint32_t v = sb & 0x7Fu;
+      neg = (sb & 0x80u) != 0;
+      if (v == 0x7Fu) {
+        record_error(err, FP4MOE_ERR_INVALID_ARG);
+        zero = true;
+      } else if (v == 0) {
+        zero = true;
+      } else if (v >= 8) {
+        code = v + 16;                          // normal: exponent + 2
+      } else {
+        const int msb = 31 - __clz(v);           // subnormal m * 2^-9
+        code = static_cast<uint32_t>((msb << 3) | ((v << (3 - msb)) & 7u));
+      }
+    } else {
+      if (sb == 0xFFu) {
+        record_error(err, FP4MOE_ERR_INVALID_ARG);
+        zero = true;
+      } else {
+        const int bm = bmax[e];
+        code = (static_cast<int>(sb) >= bm - 126)
+                   ? static_cast<uint32_t>(static_cast<int>(sb) - bm + 254)
+                   : 0u;
+      }
+    }
+    for (int i = g * gran; i < (g + 1) * gran; ++i) {
+      if (zero) codes[i] = 0;
+      else if (neg) codes[i] ^= 8u;
+    }
+    tp[kTileDataBytes + r * ng + g] = static_cast<uint8_t>(code);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 o;
+    o.x = pack8(codes + 32 * h + 0);
+    o.y = pack8(codes + 32 * h + 8);
+    o.z = pack8(codes + 32 * h + 16);
+    o.w = pack8(codes + 32 * h + 24);
+    *reinterpret_cast<uint4*>(tp + h * 2048 + r * 16) = o;
+  }
+}
+
+__global__ void alpha_kernel(const float* __restrict__ gs,
+                             const int32_t* __restrict__ bmax, int E, int gran,
+                             float* __restrict__ alpha) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  alpha[e] = (gran == 16) ? gs[e] * 128.0f : ldexpf(gs[e], bmax[e] - 128);
+}
+
+}  // namespace
+
+// ============================================================== launchers
+
+cudaError_t launch_requant(const uint8_t* fp4, const uint8_t* s16,
+                           int64_t rows, int64_t K, uint8_t* fp4_out,
+                           uint8_t* s32_out, int* err, cudaStream_t st) {
+  const int64_t groups = rows * (K / 32);
+  if (groups == 0) return cudaSuccess;
+  const int64_t want = (groups + 255) / 256;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, num_sms() * 8));
+  requant_kernel<<<blocks, 256, 0, st>>>(fp4, s16, groups, fp4_out, s32_out,
+                                         err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t T, int64_t K,
+                             uint8_t* xq, uint8_t* xs, int* err,
+                             cudaStream_t st) {
+  const int64_t groups = T * (K / 32);
+  if (groups == 0) return cudaSuccess;
+  const int64_t want = (groups + 255) / 256;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, num_sms() * 8));
+  act_quant_kernel<<<blocks, 256, 0, st>>>(x, groups, xq, xs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h_fp8_round(const float* h, int64_t rows, int64_t I,
+                               uint16_t* out, cudaStream_t st) {
+  const int64_t groups = rows * (I / 32);
+  if (groups == 0) return cudaSuccess;
+  const int64_t want = (groups + 255) / 256;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, num_sms() * 8));
+  h_fp8_round_kernel<<<blocks, 256, 0, st>>>(h, groups, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k,
+                         int32_t* ids, float* w, int32_t* hist, int* err,
+                         cudaStream_t st) {
+  const int nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
+  if (nblk == 0) return cudaSuccess;
+  const int epl = (E + 31) / 32;
+#define FP4MOE_ROUTE(N)                                                   \
+  route_kernel<N><<<nblk, kTokPerBlk * 32, 0, st>>>(logits, T, E, k, ids, w, \
+                                                    hist, err)
+  if (epl <= 1) FP4MOE_ROUTE(1);
+  else if (epl <= 2) FP4MOE_ROUTE(2);
+  else if (epl <= 4) FP4MOE_ROUTE(4);
+  else if (epl <= 8) FP4MOE_ROUTE(8);
+  else if (epl <= 16) FP4MOE_ROUTE(16);
+  else FP4MOE_ROUTE(32);
+#undef FP4MOE_ROUTE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(int T, int E, const int32_t* hist, int32_t* base,
+                        int32_t* counts, int32_t* offsets, int32_t* cstart,
+                        int chunk_max, cudaStream_t st) {
+  const int nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
+  scan_kernel<<<1, 1024, 0, st>>>(nblk, E, hist, base, counts, offsets, cstart,
+                                  chunk_max);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
+                           const int32_t* base, int32_t* perm, int32_t* inv,
+                           const void* x, const uint8_t* xs, int K,
+                           int act_mode, uint16_t* xperm, cudaStream_t st) {
+  const int nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
+  if (nblk == 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(16) * E * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(
+        scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv, x, xs,
+                                          K, act_mode, xperm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
+                           int T, int k, int K, uint16_t* y, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, 256, 0, st>>>(o, inv, w, k, K, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_max(const uint8_t* s, int E, int64_t per_expert,
+                             int32_t* bmax, int* err, cudaStream_t st) {
+  const int bx = static_cast<int>(std::min<int64_t>((per_expert + 255) / 256, 64));
+  scale_max_kernel<<<dim3(bx, E), 256, 0, st>>>(s, per_expert, bmax, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const uint8_t* w, const uint8_t* s, int E, int N,
+                        int Kd, int gran, bool gated, int layout,
+                        const int32_t* bmax, uint8_t* out, int* err,
+                        cudaStream_t st) {
+  const int64_t tiles =
+      static_cast<int64_t>(E) * (N / kTileN) * (Kd / kTileK);
+  if (tiles == 0) return cudaSuccess;
+  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  pack_kernel<<<static_cast<unsigned>(tiles), 128, 0, st>>>(
+      w, s, E, N, Kd, gran, gated ? 1 : 0, layout, bmax, out, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E, int gran,
+                         float* alpha, cudaStream_t st) {
+  alpha_kernel<<<(E + 255) / 256, 256, 0, st>>>(gs, bmax, E, gran, alpha);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4moe

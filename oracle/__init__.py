@@ -59,7 +59,7 @@ class _OrcMoe(ctypes.Structure):
         ("nthreads", ctypes.c_int32),
         ("x_bf16", ctypes.c_void_p), ("xq", ctypes.c_void_p),
         ("xs", ctypes.c_void_p), ("logits", ctypes.c_void_p),
-        ("T", ctypes.c_int64),
+        ("T", ctypes.c_int64), ("h_out", ctypes.c_void_p),
     ]
 
 
@@ -100,6 +100,12 @@ def lib() -> ctypes.CDLL:
             L.orc_act_quant.argtypes = [ctypes.c_void_p, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_void_p,
                                         ctypes.c_void_p]
+            L.orc_round_intermediate.restype = ctypes.c_int
+            L.orc_round_intermediate.argtypes = [ctypes.c_void_p,
+                                                 ctypes.c_int64, ctypes.c_int,
+                                                 ctypes.c_void_p]
+            L.orc_fp8_group_exponent.restype = ctypes.c_int
+            L.orc_fp8_group_exponent.argtypes = [ctypes.c_void_p]
             L.orc_moe_rows.restype = ctypes.c_int
             L.orc_moe_rows.argtypes = [ctypes.POINTER(_OrcMoe),
                                        ctypes.c_void_p, ctypes.c_int64,
@@ -207,10 +213,27 @@ def act_quant(x_bf16: np.ndarray):
     return q, s
 
 
+def round_intermediate(h: np.ndarray, act_mode: int) -> np.ndarray:
+    """h rounded as stored between FC1 and FC2 (bf16, or E4M3 x UE8M0/32)."""
+    h = np.ascontiguousarray(h, dtype=np.float64)
+    out = np.empty_like(h)
+    if lib().orc_round_intermediate(_ptr(h), h.size, act_mode, _ptr(out)):
+        raise ValueError("oracle round_intermediate rejected its input")
+    return out
+
+
+def fp8_group_exponent(h32: np.ndarray) -> int:
+    h32 = np.ascontiguousarray(h32, dtype=np.float64)
+    assert h32.size == 32
+    return lib().orc_fp8_group_exponent(_ptr(h32))
+
+
 def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
              w13_layout, act_mode, top_k, logits, x_bf16=None, xq=None,
-             xs=None, nthreads=None) -> np.ndarray:
-    """MoE output rows y[t] in FP64 (before the final bf16 rounding), S2-S7."""
+             xs=None, nthreads=None, return_h=False):
+    """MoE output rows y[t] in FP64 (before the final bf16 rounding), S2-S7.
+
+    With return_h, also returns the unrounded intermediate h [ntok, k, I]."""
     E, twoI, kb = w13.shape
     K, I = kb * 2, twoI // 2
     T = logits.shape[0]
@@ -229,13 +252,14 @@ def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
         arrs["xq"] = np.ascontiguousarray(xq, dtype=np.uint8)
         arrs["xs"] = np.ascontiguousarray(xs, dtype=np.uint8)
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    h = np.empty((tok.size, top_k, I), dtype=np.float64) if return_h else None
     args = _OrcMoe(
         _ptr(arrs["w13"]), _ptr(arrs["w13_s"]), _ptr(arrs["w13_gs"]),
         _ptr(arrs["w2"]), _ptr(arrs["w2_s"]), _ptr(arrs["w2_gs"]),
         E, K, I, gran, w13_layout, act_mode, top_k, nthreads or cores(),
         _ptr(arrs["x_bf16"]), _ptr(arrs["xq"]), _ptr(arrs["xs"]),
-        _ptr(arrs["logits"]), T)
+        _ptr(arrs["logits"]), T, _ptr(h))
     y = np.empty((tok.size, K), dtype=np.float64)
     if lib().orc_moe_rows(ctypes.byref(args), _ptr(tok), tok.size, _ptr(y)):
         raise ValueError("oracle moe_rows rejected its input")
-    return y
+    return (y, h) if return_h else y

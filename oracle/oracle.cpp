@@ -324,6 +324,7 @@ int orc_act_quant(const uint16_t* x, int64_t T, int64_t K, uint8_t* q,
 //   o_n = gs2 * sum_i h_i * w2[n, i]
 //   y_t = sum_j w_{t,j} * o_{(t,j)}, in top-k order.  Returned in FP64; the
 //   product rounds y to bfloat16 (orc_bf16_rne gives that rounding).
+//   If h_out is set, the unrounded h of each (token, slot) is stored there.
 // act_mode 0 reads x_bf16 [T, K]; act_mode 1 reads xq [T, K] (E4M3) and
 // xs [T, K/32] (UE8M0).
 struct OrcMoe {
@@ -339,6 +340,7 @@ struct OrcMoe {
   const uint8_t* xs;
   const float* logits;
   int64_t T;
+  double* h_out;  // optional [ntok, top_k, I]: h before its rounding
 };
 
 static double weight_value(const uint8_t* w, const uint8_t* s, int gran,
@@ -374,6 +376,25 @@ static void round_intermediate(std::vector<double>& h, int act_mode) {
     for (int i = 0; i < 32; ++i)
       h[g * 32 + i] = orc_e4m3_value(orc_e4m3_rne_sat(h[g * 32 + i] / sc)) * sc;
   }
+}
+
+// Rounds n values of h the way the intermediate is stored (act_mode 0:
+// bfloat16; act_mode 1: E4M3 with a per-32 UE8M0 scale, n % 32 == 0).
+int orc_round_intermediate(const double* h, int64_t n, int act_mode,
+                           double* out) {
+  if (act_mode == 1 && n % 32) return 1;
+  std::vector<double> v(h, h + n);
+  round_intermediate(v, act_mode);
+  std::copy(v.begin(), v.end(), out);
+  return 0;
+}
+
+// The UE8M0 exponent (byte - 127) the FP8 rounding picks for 32 values.
+int orc_fp8_group_exponent(const double* h32) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(h32[i]));
+  int e = (amax == 0.0) ? 0 : min_pow2_exponent(amax, 448.0);
+  return std::min(254, std::max(0, e + 127)) - 127;
 }
 
 // y_out: [ntok, K] FP64 for the tokens listed in `tokens`.
@@ -413,6 +434,8 @@ int orc_moe_rows(const OrcMoe* a, const int64_t* tokens, int64_t ntok,
         u[i] = gs13 * row_dot(w13, w13s, a->gran, K, up0 + i, x.data());
         h[i] = g[i] / (1.0 + std::exp(-g[i])) * u[i];
       });
+      if (a->h_out)
+        std::copy(h.begin(), h.end(), a->h_out + (n * a->top_k + j) * I);
       round_intermediate(h, a->act_mode);
       parallel_for(K, a->nthreads, [&](int64_t c) {
         o[c] = gs2 * row_dot(w2, w2s, a->gran, I, c, h.data());

@@ -7,23 +7,24 @@ GEMM, SwiGLU or combine).
 
 Weights are drawn FP32 N(0, 0.02) and then encoded as NVFP4 (E2M1 codes, one
 E4M3 scale per 16 K-elements, one FP32 global scale per expert matrix), which
-is the input format the pages' checkpoints arrive in.  That encoding is an
-input recipe, not a step of the method: it rounds to nearest with ties away
-from zero through table look-ups, and neither the oracle nor the CUDA library
-calls it.  The recipe:
+is the input format the pages' checkpoints arrive in.  That encoding (in
+synth.c) is an input recipe, not a step of the method: it rounds to nearest
+with ties away from zero through table look-ups, and neither the oracle nor
+the CUDA library calls it.  The recipe:
 
     gs   = amax(W_e) / (6 * 448)                    per expert matrix
     s16  = nearest E4M3 to amax(group16) / (6 * gs)
     code = nearest E2M1 to w / (s16 * gs)            (s16 == 0 -> code 0)
 
-Streams: ``numpy.random.SeedSequence(seed).spawn`` gives one child per
-(tensor, expert), so generation parallelises over experts and stays
-reproducible.
+Streams: weights use a counter-based generator keyed by (seed, expert), so
+experts generate in parallel and reproducibly; logits and activations use
+``numpy.random.SeedSequence(seed).spawn`` children.
 """
 from __future__ import annotations
 
+import ctypes
 import os
-from concurrent.futures import ThreadPoolExecutor
+import subprocess
 from dataclasses import dataclass
 
 import numpy as np
@@ -105,22 +106,40 @@ SMALL_REQUANT = RequantConfig("small_requant_E3_N100_K480", 3 * 100, 480, 3,
 CONFIGS = {c.name: c for c in (TINY, DECODE, DECODE_SKEW, PREFILL, FP8,
                                SMALL_DECODE, SMALL_PREFILL, SMALL_FP8)}
 
-# --------------------------------------------------------------- tables
-# Non-negative finite values of the two 8/4-bit formats, indexed by code.
+# --------------------------------------------------------------- weights
+# The weight generator is portable C (synth.c): SplitMix64 counters, Box-Muller
+# normals and the NVFP4 encoding recipe, threaded over experts.
 
-_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
-_E2M1_MID = (_E2M1_POS[1:] + _E2M1_POS[:-1]) / 2
-
-
-def _e4m3_pos_table() -> np.ndarray:
-    b = np.arange(127)
-    e, m = b >> 3, b & 7
-    return np.where(e == 0, m / 8.0 * 2.0 ** -6,
-                    (1 + m / 8.0) * 2.0 ** (e - 7.0))
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libsynth.so")
+_lib = None
 
 
-_E4M3_POS = _e4m3_pos_table()
-_E4M3_MID = (_E4M3_POS[1:] + _E4M3_POS[:-1]) / 2
+def build(force: bool = False) -> str:
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread",
+                    "-ffp-contract=off", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _clib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        L.synth_nvfp4_weights.restype = ctypes.c_int
+        L.synth_nvfp4_weights.argtypes = [
+            ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_float, ctypes.c_double, ctypes.c_float, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        _lib = L
+    return _lib
 
 
 def _threads() -> int:
@@ -145,52 +164,19 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
 
 
-def encode_nvfp4(w: np.ndarray):
-    """Input recipe: FP32 [N, Kd] -> (codes packed [N, Kd/2], E4M3 [N, Kd/16], gs).
-
-    Nearest with ties away from zero (see the module docstring)."""
-    N, Kd = w.shape
-    a = np.abs(w)
-    amax = float(a.max())
-    gs = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
-    ga = a.reshape(N, Kd // 16, 16).max(axis=2).astype(np.float64)
-    t = ga / (6.0 * float(gs))
-    si = np.searchsorted(_E4M3_MID, t, side="right").astype(np.uint8)  # 0..126
-    sval = _E4M3_POS[si] * float(gs)                                      # [N, G]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        y = w.reshape(N, Kd // 16, 16) / sval[:, :, None]
-    y = np.where(sval[:, :, None] > 0, y, 0.0)
-    mag = np.searchsorted(_E2M1_MID, np.abs(y), side="right").astype(np.uint8)
-    codes = (mag | np.where(y < 0, np.uint8(8), np.uint8(0))).reshape(N, Kd)
-    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
-    return packed, si, gs
-
-
-def _draw_expert_matrix(seq, N, Kd, std=0.02, outlier_p=0.0, outlier_mul=1.0):
-    g = _rng(seq)
-    w = g.standard_normal((N, Kd), dtype=np.float32)
-    w *= np.float32(std)
-    if outlier_p > 0:
-        mask = g.random((N, Kd), dtype=np.float32) < outlier_p
-        w[mask] *= np.float32(outlier_mul)
-    return w
-
-
 def nvfp4_weights(E: int, N: int, Kd: int, seed: int, outlier_p=0.0,
                   outlier_mul=1.0, threads: int | None = None):
-    """E expert matrices [N, Kd] drawn N(0, 0.02) and encoded as NVFP4 g16."""
+    """E expert matrices [N, Kd] drawn N(0, 0.02) and encoded as NVFP4 g16:
+    codes [E, N, Kd/2] u8, E4M3 scales [E, N, Kd/16] u8, gs [E] f32."""
     codes = np.empty((E, N, Kd // 2), dtype=np.uint8)
     scales = np.empty((E, N, Kd // 16), dtype=np.uint8)
     gs = np.empty(E, dtype=np.float32)
-    seqs = np.random.SeedSequence(seed).spawn(E)
-
-    def one(e):
-        w = _draw_expert_matrix(seqs[e], N, Kd, outlier_p=outlier_p,
-                                outlier_mul=outlier_mul)
-        codes[e], scales[e], gs[e] = encode_nvfp4(w)
-
-    with ThreadPoolExecutor(threads or _threads()) as ex:
-        list(ex.map(one, range(E)))
+    rc = _clib().synth_nvfp4_weights(
+        seed & 0xFFFFFFFFFFFFFFFF, E, N, Kd, 0.02, outlier_p, outlier_mul,
+        codes.ctypes.data, scales.ctypes.data, gs.ctypes.data,
+        threads or _threads())
+    if rc:
+        raise ValueError("bad weight shape")
     return codes, scales, gs
 
 

@@ -1,0 +1,250 @@
+"""GPU parity of prepare_weights (layout round trip) and moe_forward (S2-S7)
+against the FP64 oracle, within |gpu - oracle| <= 2^-7|oracle| + 1e-3 rms."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp4_02_gb300 as fp4
+import synth
+from _util import (bf16_tensor, check_moe, decode_packed, dequant_reference,
+                   requant_weights_oracle, weights_for)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    fp4.build()
+    fp4.load()
+    assert fp4.last_device_error() == fp4.OK
+
+
+def to_dev(w):
+    return {k: torch.from_numpy(np.ascontiguousarray(v)).cuda()
+            for k, v in w.items()}
+
+
+def prepare(w, gran=16, layout=0, act=fp4.ACT_BF16):
+    d = to_dev(w)
+    p = fp4.prepare_weights(d["w13"], d["w13_s"], d["w13_gs"], d["w2"],
+                            d["w2_s"], d["w2_gs"], gran_k=gran,
+                            w13_layout=layout, act_mode=act)
+    del d
+    return p
+
+
+def swap_halves(w, I):
+    out = dict(w)
+    out["w13"] = np.ascontiguousarray(
+        np.concatenate([w["w13"][:, I:], w["w13"][:, :I]], 1))
+    out["w13_s"] = np.ascontiguousarray(
+        np.concatenate([w["w13_s"][:, I:], w["w13_s"][:, :I]], 1))
+    return out
+
+
+def gpu_forward(p, acts, k, act):
+    """moe_forward on device tensors; returns y and the workspace."""
+    logits = torch.from_numpy(acts["logits"]).cuda()
+    xb = bf16_tensor(acts["x_bf16"])
+    T = logits.shape[0]
+    ws = torch.empty(max(fp4.moe_workspace_size(p, T, k), 256),
+                     dtype=torch.uint8, device="cuda")
+    if act == fp4.ACT_BF16:
+        y = fp4.moe_forward(xb, None, logits, p, k, workspace=ws)
+    else:
+        xq, xs = fp4.act_quant(xb)
+        y = fp4.moe_forward(xq, xs, logits, p, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == fp4.OK
+    return y, ws
+
+
+def check_against_oracle(orc, cfg, w, acts, p, y, ws, tokens, layout=0,
+                         gran=16, what=None):
+    """Oracle rows for `tokens`, then the two-level (h, y) parity check."""
+    tokens = list(tokens)
+    if cfg.act == "fp8":
+        w_used = requant_weights_oracle(orc, w, cfg.E, cfg.K, cfg.I)
+        xq, xs = orc.act_quant(acts["x_bf16"])
+        ref_y, ref_h = orc.moe_rows(tokens, **w_used, gran=32,
+                                    w13_layout=layout, act_mode=1,
+                                    top_k=cfg.top_k, logits=acts["logits"],
+                                    xq=xq, xs=xs, return_h=True)
+        gran, act = 32, 1
+    else:
+        w_used, act = w, 0
+        ref_y, ref_h = orc.moe_rows(tokens, **w, gran=gran,
+                                    w13_layout=layout, act_mode=0,
+                                    top_k=cfg.top_k, logits=acts["logits"],
+                                    x_bf16=acts["x_bf16"], return_h=True)
+    return check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, w_used,
+                     gran, act, acts["logits"], what or cfg.name)
+
+
+# ------------------------------------------------------------------ layout
+
+@pytest.mark.parametrize("gran,act", [(16, fp4.ACT_BF16), (16, fp4.ACT_FP8),
+                                      (32, fp4.ACT_BF16)])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_prepare_layout_roundtrip(orc, gran, act, layout):
+    E, K, I = 3, 256, 384
+    w = synth.moe_weights(synth.MoeConfig("rt", E, K, I, 1, 1, weight_seed=77))
+    if gran == 32:
+        w = requant_weights_oracle(orc, w, E, K, I)
+    p = prepare(w, gran=gran, layout=layout, act=act)
+    bufs = p.buffers()
+    d = p.desc
+    if act == fp4.ACT_FP8 and gran == 16:
+        ref_w = requant_weights_oracle(orc, w, E, K, I)
+        rg = 32
+    else:
+        ref_w, rg = w, gran
+    assert d.gran_k == rg
+    ref13 = dequant_reference(ref_w["w13"], ref_w["w13_s"], rg, ref_w["w13_gs"])
+    ref2 = dequant_reference(ref_w["w2"], ref_w["w2_s"], rg, ref_w["w2_gs"])
+    got13 = decode_packed(bufs["w13"].numpy(), E, 2 * I, K, rg, d.scale_mul,
+                          d.scale_add, bufs["alpha13"].numpy(), True, I,
+                          layout)
+    got2 = decode_packed(bufs["w2"].numpy(), E, K, I, rg, d.scale_mul,
+                         d.scale_add, bufs["alpha2"].numpy(), False)
+    # Exact: every packed value equals e2m1 * scale * gs of the source.
+    np.testing.assert_array_equal(got13, ref13)
+    np.testing.assert_array_equal(got2, ref2)
+
+
+def test_prepare_rejects_nan_scale():
+    E, K, I = 2, 128, 128
+    w = synth.moe_weights(synth.MoeConfig("nan", E, K, I, 1, 1, weight_seed=5))
+    w["w2_s"][1, 7, 3] = 0x7F
+    with pytest.raises(fp4.FP4MoEError) as ei:
+        prepare(w)
+    assert ei.value.code == fp4.ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------- MoE small
+
+SMALL = [synth.TINY, synth.SMALL_DECODE, synth.SMALL_PREFILL, synth.SMALL_FP8]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_moe_small_configs_all_tokens(orc, cfg, layout):
+    w = weights_for(cfg)
+    if layout == 1:
+        w = swap_halves(w, cfg.I)
+    acts = synth.moe_activations(cfg)
+    act = fp4.ACT_FP8 if cfg.act == "fp8" else fp4.ACT_BF16
+    p = prepare(w, layout=layout, act=act)
+    y, ws = gpu_forward(p, acts, cfg.top_k, act)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(cfg.T),
+                         layout=layout)
+
+
+def test_moe_group32_weights_bf16_activations(orc):
+    # W4A16 over MX (UE8M0 group32) weights, no requant on the GPU side.
+    cfg = synth.SMALL_DECODE
+    w32 = requant_weights_oracle(orc, weights_for(cfg), cfg.E, cfg.K, cfg.I)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w32, gran=32)
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    check_against_oracle(orc, cfg, w32, acts, p, y, ws, range(cfg.T), gran=32,
+                         what="group32 bf16")
+
+
+@pytest.mark.parametrize("T", [1, 2, 17, 300])
+def test_moe_token_counts(orc, T):
+    base = synth.SMALL_DECODE
+    cfg = synth.MoeConfig("t", base.E, base.K, base.I, T, base.top_k,
+                          weight_seed=base.weight_seed, input_seed=900 + T)
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w)
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=f"T={T}")
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_moe_hot_experts_get_every_token(orc, k):
+    # The first k experts win every token: 600 tokens per expert, so each
+    # expert is split into several token chunks.
+    cfg = synth.MoeConfig("hot", 8, 768, 384, 600, k, weight_seed=3002,
+                          input_seed=4242)
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    acts["logits"][:, 0] += 100.0
+    acts["logits"][:, 1] += 99.0
+    p = prepare(w)
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(cfg.T),
+                         what=f"hot experts k={k}")
+
+
+def test_moe_zero_tokens_is_noop():
+    cfg = synth.TINY
+    p = prepare(weights_for(cfg))
+    x = torch.empty(0, cfg.K, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty(0, cfg.E, dtype=torch.float32, device="cuda")
+    y = fp4.moe_forward(x, None, logits, p, cfg.top_k,
+                        workspace=torch.empty(256, dtype=torch.uint8,
+                                              device="cuda"))
+    assert y.shape == (0, cfg.K)
+
+
+def test_moe_deterministic_and_host_api(orc):
+    cfg = synth.SMALL_PREFILL
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w)
+    y1, _ = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    y2, _ = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # the host-buffer entry point gives the same bits
+    xh = torch.from_numpy(acts["x_bf16"].view(np.int16)).view(
+        torch.bfloat16).pin_memory()
+    lh = torch.from_numpy(acts["logits"]).pin_memory()
+    yh = torch.empty(cfg.T, cfg.K, dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(fp4.moe_workspace_size_host(p, cfg.T, cfg.top_k),
+                     dtype=torch.uint8, device="cuda")
+    fp4.moe_forward_host(xh, None, lh, p, cfg.top_k, yh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(yh.view(torch.int16), y1.cpu().view(torch.int16))
+
+
+def test_moe_workspace_too_small():
+    cfg = synth.TINY
+    p = prepare(weights_for(cfg))
+    acts = synth.moe_activations(cfg)
+    need = fp4.moe_workspace_size(p, cfg.T, cfg.top_k)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp4.FP4MoEError) as ei:
+        fp4.moe_forward(bf16_tensor(acts["x_bf16"]), None,
+                        torch.from_numpy(acts["logits"]).cuda(), p,
+                        cfg.top_k, workspace=ws)
+    assert ei.value.code == fp4.ERR_WORKSPACE_TOO_SMALL
+
+
+# ---------------------------------------------------------- MoE full size
+
+def _sample_tokens(T, n, seed):
+    g = np.random.default_rng(seed)
+    s = set(g.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
+    return sorted(s)
+
+
+@pytest.mark.parametrize("cfg,n", [(synth.DECODE, 64), (synth.DECODE_SKEW, 64),
+                                   (synth.PREFILL, 24), (synth.FP8, 24)],
+                         ids=lambda c: getattr(c, "name", str(c)))
+def test_moe_full_size_sampled(orc, cfg, n):
+    """Full-size workloads in the benchmark's launch configuration; the
+    oracle recomputes a sample of output rows one token at a time."""
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    act = fp4.ACT_FP8 if cfg.act == "fp8" else fp4.ACT_BF16
+    p = prepare(w, act=act)
+    y, ws = gpu_forward(p, acts, cfg.top_k, act)
+    toks = _sample_tokens(cfg.T, n, 99)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, toks)
+    p.free()
