@@ -7,14 +7,20 @@
 // W is dequantized FP4 -> bf16 into shared memory in the 128-byte swizzled
 // K-major layout; X (bf16 activations in expert-major order) arrives by TMA
 // in the same layout.  Warp roles, one CTA per SM, persistent over units:
-//   warp 0     : producer -- bulk copy of the packed FP4 tile + TMA of the
-//                token rows for each 64-wide K step into a ring of stages;
-//   warp 1     : TMEM allocation and the single UMMA-issuing thread
-//                (kind::f16, M = 128, N = tokens rounded up to 16, K = 16);
-//   warps 2..9 : dequantizers (warp w owns rows 32*(w%4).. and one 32-wide K
-//                half of each step), then the epilogue reading TMEM.
-// All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
-// the device status word and the CTA winds down and frees its TMEM.
+//   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
+//                 (one per 64-wide K step) into a deep ring of F stages;
+//   warp 1      : TMEM allocation and the single UMMA-issuing thread
+//                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16);
+//   warp 2      : activation producer -- TMA of the token rows of each K step
+//                 into the B half of a ring of A/B stages;
+//   warps 3..10 : dequantizers (warp w owns rows 32*(w%4).. and one 32-wide
+//                 K half of each step), writing the A half of the A/B stage;
+//   warps 11..14: epilogue, reading one of two TMEM accumulators while the
+//                 MMA fills the other.
+// The weight ring runs ahead of the A/B ring, so weight bytes in flight are
+// bounded by the F ring depth, not by the (larger) operand stages.  All waits
+// are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in the device
+// status word and the CTA winds down and frees its TMEM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,20 +28,26 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kWarps = 10;
+constexpr int kWarps = 15;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpFProd = 0, kWarpMma = 1, kWarpBProd = 2, kWarpDq0 = 3,
+              kWarpEpi0 = 11;
 constexpr uint32_t kABytes = kTileN * kTileK * 2;  // 16 KB bf16 tile
-constexpr uint32_t kFBytes = 5120;  // >= largest packed tile, 1 KB multiple
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kFBytes = 4608;                 // >= largest packed tile
+constexpr uint32_t kTmemCols = 512;                // two 256-column buffers
 
 template <int NT>
 struct Cfg {
   static constexpr uint32_t kBBytes = NT * 128;  // NT rows x 64 bf16
-  static constexpr uint32_t kStage = kABytes + kBBytes + kFBytes;
-  static constexpr int kStages = NT >= 256 ? 4 : (NT >= 128 ? 5 : 7);
-  static constexpr uint32_t kBarOff = kStage * kStages;
-  static constexpr uint32_t kSmem = kBarOff + 256 + 1024;
+  static constexpr uint32_t kABStage = kABytes + kBBytes;
+  static constexpr int kSA = NT >= 256 ? 4 : 3;
+  static constexpr int kSF = NT >= 256 ? 6 : 32;
+  static constexpr uint32_t kFOff = kABStage * kSA;
+  static constexpr uint32_t kBarOff = kFOff + kFBytes * kSF;
+  static constexpr int kNumBars = 2 * kSF + 3 * kSA + 5;
+  static constexpr uint32_t kSmem = kBarOff + 8 * kNumBars + 16 + 1024;
 };
 
 struct Unit {
@@ -88,34 +100,42 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
   using C = Cfg<NT>;
-  constexpr int S = C::kStages;
+  constexpr int SA = C::kSA, SF = C::kSF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bars = sbase + C::kBarOff;
-  auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto aready_bar = [&](int s) { return bars + 8u * (S + s); };
-  auto empty_bar = [&](int s) { return bars + 8u * (2 * S + s); };
-  const uint32_t acc_full = bars + 8u * (3 * S);
-  const uint32_t acc_empty = bars + 8u * (3 * S + 1);
-  const uint32_t done_bar = bars + 8u * (3 * S + 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 8 * (3 * S + 3));
+  auto fullF = [&](int s) { return bars + 8u * s; };
+  auto emptyF = [&](int s) { return bars + 8u * (SF + s); };
+  auto fullB = [&](int s) { return bars + 8u * (2 * SF + s); };
+  auto aready = [&](int s) { return bars + 8u * (2 * SF + SA + s); };
+  auto emptyAB = [&](int s) { return bars + 8u * (2 * SF + 2 * SA + s); };
+  auto accFull = [&](int b) { return bars + 8u * (2 * SF + 3 * SA + b); };
+  auto accEmpty = [&](int b) { return bars + 8u * (2 * SF + 3 * SA + 2 + b); };
+  const uint32_t done_bar = bars + 8u * (2 * SF + 3 * SA + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 8 * C::kNumBars);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(aready_bar(s), kDqWarps);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < SF; ++s) {
+      mbar_init(fullF(s), 1);
+      mbar_init(emptyF(s), kDqWarps);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kDqWarps);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(fullB(s), 1);
+      mbar_init(aready(s), kDqWarps);
+      mbar_init(emptyAB(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accFull(b), 1);
+      mbar_init(accEmpty(b), kEpiWarps);
+    }
     mbar_init(done_bar, 1);
     fence_barrier_init();
-    prefetch_tensormap(&tmB);
   }
-  if (warp == 1) {
+  if (warp == kWarpBProd && lane == 0) prefetch_tensormap(&tmB);
+  if (warp == kWarpMma) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -125,121 +145,154 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int total = a.nblocks * __ldg(a.cstart + a.E);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == kWarpFProd) {
+    // ------------------------------------------------- weight producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit U = decode_unit(a, u);
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
-        const int nbox = (U.ntok + 15) >> 4;
-        const uint32_t bytes = a.tile_bytes + nbox * 2048u;
         for (int ks = 0; ks < a.ksteps; ++ks) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u)) { ok = false; break; }
-          const uint32_t st = sbase + stage * C::kStage;
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
-          bulk_load(st + kABytes + C::kBBytes, wt + static_cast<int64_t>(ks) * a.tile_bytes,
-                    a.tile_bytes, full_bar(stage));
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(st + kABytes + b * 2048u, &tmB, ks * kTileK, U.row0 + 16 * b,
-                        full_bar(stage));
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (!mbar_wait(emptyF(s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(fullF(s), a.tile_bytes);
+          bulk_load(sbase + C::kFOff + s * kFBytes,
+                    wt + static_cast<int64_t>(ks) * a.tile_bytes, a.tile_bytes, fullF(s));
+          issued |= 1u << (s & 31);
+          issued_ph = (issued_ph & ~(1u << (s & 31))) | (ph << (s & 31));
+          if (++s == SF) { s = 0; ph ^= 1u; }
         }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
       // Copies still in flight must land before the CTA exits.
-      for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) mbar_wait(full_bar(s), (issued_parity >> s) & 1u);
+      for (int t = 0; t < SF && t < 32; ++t)
+        if ((issued >> t) & 1u) mbar_wait(fullF(t), (issued_ph >> t) & 1u);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpBProd) {
+    // --------------------------------------------- activation producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit U = decode_unit(a, u);
+        const int nbox = (U.ntok + 15) >> 4;
+        for (int ks = 0; ks < a.ksteps; ++ks) {
+          if (!mbar_wait(emptyAB(s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(fullB(s), nbox * 2048u);
+          const uint32_t dst = sbase + s * C::kABStage + kABytes;
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(dst + b * 2048u, &tmB, ks * kTileK, U.row0 + 16 * b, fullB(s));
+          issued |= 1u << s;
+          issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+          if (++s == SA) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
+      for (int t = 0; t < SA; ++t)
+        if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
+    }
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int s = 0, buf = 0;
+      uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit U = decode_unit(a, u);
         const uint32_t n = static_cast<uint32_t>((U.ntok + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, n);
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u)) { ok = false; break; }
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * 256u;
+        if (!mbar_wait(accEmpty(buf), acc_ph ^ 1u)) { ok = false; break; }
         tc_fence_after();
         for (int ks = 0; ks < a.ksteps; ++ks) {
-          if (!mbar_wait(aready_bar(stage), phase)) { ok = false; break; }
+          if (!mbar_wait(fullB(s), ph) || !mbar_wait(aready(s), ph)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = sbase + stage * C::kStage;
+          const uint32_t st = sbase + s * C::kABStage;
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)
-            umma_f16(tmem, sw128_kmajor_desc(st + kk * 32),
+            umma_f16(d_tmem, sw128_kmajor_desc(st + kk * 32),
                      sw128_kmajor_desc(st + kABytes + kk * 32), idesc,
                      (ks | kk) != 0 ? 1u : 0u);
-          umma_commit(empty_bar(stage));
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          umma_commit(emptyAB(s));
+          if (++s == SA) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(acc_full);
-        acc_phase ^= 1u;
+        umma_commit(accFull(buf));
+        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
       // Let every issued MMA finish before TMEM is released.
       umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) record_error(a.err, FP4MOE_ERR_TIMEOUT);
     }
-  } else {
-    // ------------------------------------------------ dequant + epilogue
-    const int dq = warp - 2;          // 0..7
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
+  } else if (warp < kWarpEpi0) {
+    // ---------------------------------------------------------- dequant
+    const int dq = warp - kWarpDq0;   // 0..7
+    const int q = warp & 3;           // row quarter
     const int khalf = dq >> 2;        // 32-wide K half of each step
     const int r = 32 * q + lane;      // weight row in the tile
     const uint32_t smul = a.smul, sadd = a.sadd;
     const uint32_t a_row_off = (r >> 3) * 1024u + (r & 7) * 128u;
-    int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    const uint32_t sw = r & 7, cb = 4 * khalf;
+    int sf = 0, sa = 0;
+    uint32_t phf = 0, pha = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit U = decode_unit(a, u);
       for (int ks = 0; ks < a.ksteps; ++ks) {
-        if (!mbar_wait(full_bar(stage), phase)) { ok = false; break; }
-        const uint8_t* f = smem + stage * C::kStage + kABytes + C::kBBytes;
+        if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
+        const uint8_t* f = smem + C::kFOff + sf * kFBytes;
         const uint4 d = *reinterpret_cast<const uint4*>(f + khalf * 2048 + r * 16);
         uint32_t c0, c1;
         if (a.gran == 16) {
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(f + kTileDataBytes + r * 4 + khalf * 2);
+          const uint32_t sc =
+              *reinterpret_cast<const uint16_t*>(f + kTileDataBytes + r * 4 + khalf * 2);
           c0 = sc & 0xFFu;
           c1 = sc >> 8;
         } else {
           c0 = c1 = f[kTileDataBytes + r * 2 + khalf];
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyF(sf));
+        if (++sf == SF) { sf = 0; phf ^= 1u; }
         uint32_t s0 = c0 * smul + sadd, s1 = c1 * smul + sadd;
         s0 |= s0 << 16;
         s1 |= s1 << 16;
-        const uint32_t arow = sbase + stage * C::kStage + a_row_off;
-        const uint32_t sw = r & 7;
-        const uint32_t cb = 4 * khalf;
-        st_shared_v4(arow + (((cb + 0) ^ sw) << 4), dequant8(d.x, s0));
-        st_shared_v4(arow + (((cb + 1) ^ sw) << 4), dequant8(d.y, s0));
-        st_shared_v4(arow + (((cb + 2) ^ sw) << 4), dequant8(d.z, s1));
-        st_shared_v4(arow + (((cb + 3) ^ sw) << 4), dequant8(d.w, s1));
+        const uint4 w0 = dequant8(d.x, s0), w1 = dequant8(d.y, s0);
+        const uint4 w2 = dequant8(d.z, s1), w3 = dequant8(d.w, s1);
+        if (!mbar_wait(emptyAB(sa), pha ^ 1u)) { ok = false; break; }
+        const uint32_t arow = sbase + sa * C::kABStage + a_row_off;
+        st_shared_v4(arow + (((cb + 0) ^ sw) << 4), w0);
+        st_shared_v4(arow + (((cb + 1) ^ sw) << 4), w1);
+        st_shared_v4(arow + (((cb + 2) ^ sw) << 4), w2);
+        st_shared_v4(arow + (((cb + 3) ^ sw) << 4), w3);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aready_bar(stage));
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive(aready(sa));
+        if (++sa == SA) { sa = 0; pha ^= 1u; }
       }
-      if (!ok) break;
-      // ---- epilogue: columns in chunks of 16, alternating between the two
-      // groups of four warps.
-      if (!mbar_wait(acc_full, acc_phase)) { ok = false; break; }
+    }
+    if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int r = 32 * q + lane;      // weight row in the tile
+    int buf = 0;
+    uint32_t acc_ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit U = decode_unit(a, u);
+      if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
       const int nchunks = (U.ntok + 15) >> 4;
-      for (int j = khalf; j < nchunks; j += 2) {
+      const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                              static_cast<uint32_t>(buf) * 256u;
+      for (int j = 0; j < nchunks; ++j) {
         uint32_t v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 16 * j, v);
+        tmem_ld16(t_base + 16 * j, v);
         tmem_ld_wait();
         if (MODE == kGemmModeFc2) {
           float* o = static_cast<float*>(a.out);
@@ -275,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(accEmpty(buf));
+      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
     }
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   }
@@ -285,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // so no UMMA is still writing TMEM; free it.
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -72,51 +72,74 @@ __device__ __forceinline__ uint32_t remap8(uint32_t w, uint32_t lo, uint32_t hi,
   return __byte_perm(t0, t1, 0x6420) | ((w & 0x88888888u) ^ sx);
 }
 
+__device__ __forceinline__ void requant_group(uint4 d, uint32_t sc, uint4& o,
+                                              uint32_t& byte, int* err) {
+  const uint32_t sb0 = sc & 0xFFu, sb1 = sc >> 8;
+  if ((sb0 & 0x7Fu) == 0x7Fu || (sb1 & 0x7Fu) == 0x7Fu) {
+    record_error(err, FP4MOE_ERR_INVALID_ARG);
+    o = make_uint4(0, 0, 0, 0);
+    byte = 0xFFu;
+    return;
+  }
+  const float2 s = e4m3x2_to_f32x2(sc);
+  const float a0 = fabsf(s.x), a1 = fabsf(s.y);
+  const float amax = fmaxf(e2m1_mag(max_mag16(d.x, d.y)) * a0,
+                           e2m1_mag(max_mag16(d.z, d.w)) * a1);
+  int e = 0;
+  if (amax > 0.0f) {
+    // amax = 1.f * 2^E; 6 * 2^(E-2) = 1.5 * 2^E covers f <= 1.5.
+    const uint32_t bits = __float_as_uint(amax);
+    const int E = static_cast<int>(bits >> 23) - 127;
+    e = ((bits & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;
+  }
+  e = max(-126, min(127, e));
+  byte = static_cast<uint32_t>(e + 127);
+  // |s| / 2^e: e is in [-13, 9] for any finite non-zero group, so the power
+  // of two is a normal float.
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  uint32_t l0, h0, l1, h1;
+  build_lut(a0 * inv, l0, h0);
+  build_lut(a1 * inv, l1, h1);
+  const uint32_t sx0 = (sb0 & 0x80u) ? 0x88888888u : 0u;
+  const uint32_t sx1 = (sb1 & 0x80u) ? 0x88888888u : 0u;
+  o.x = remap8(d.x, l0, h0, sx0);
+  o.y = remap8(d.y, l0, h0, sx0);
+  o.z = remap8(d.z, l1, h1, sx1);
+  o.w = remap8(d.w, l1, h1, sx1);
+}
+
+// Each thread takes kRqUnroll groups per iteration with all loads issued
+// first, so that enough bytes are in flight to cover HBM latency.
+constexpr int kRqUnroll = 4;
+
 __global__ void __launch_bounds__(256) requant_kernel(
     const uint8_t* __restrict__ fp4, const uint8_t* __restrict__ s16,
     int64_t groups, uint8_t* __restrict__ out, uint8_t* __restrict__ s32,
     int* err) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       g < groups; g += stride) {
-    const uint4 d = __ldcs(reinterpret_cast<const uint4*>(fp4) + g);
-    const uint32_t sc = __ldcs(reinterpret_cast<const uint16_t*>(s16) + g);
-    const uint32_t sb0 = sc & 0xFFu, sb1 = sc >> 8;
-    uint4 o;
-    uint32_t byte;
-    if ((sb0 & 0x7Fu) == 0x7Fu || (sb1 & 0x7Fu) == 0x7Fu) {
-      record_error(err, FP4MOE_ERR_INVALID_ARG);
-      o = make_uint4(0, 0, 0, 0);
-      byte = 0xFFu;
-    } else {
-      const float2 s = e4m3x2_to_f32x2(sc);
-      const float a0 = fabsf(s.x), a1 = fabsf(s.y);
-      const float amax = fmaxf(e2m1_mag(max_mag16(d.x, d.y)) * a0,
-                               e2m1_mag(max_mag16(d.z, d.w)) * a1);
-      int e = 0;
-      if (amax > 0.0f) {
-        // amax = 1.f * 2^E; 6 * 2^(E-2) = 1.5 * 2^E covers f <= 1.5.
-        const uint32_t bits = __float_as_uint(amax);
-        const int E = static_cast<int>(bits >> 23) - 127;
-        e = ((bits & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;
+  for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g0 < groups; g0 += kRqUnroll * stride) {
+    uint4 d[kRqUnroll];
+    uint32_t sc[kRqUnroll];
+#pragma unroll
+    for (int i = 0; i < kRqUnroll; ++i) {
+      const int64_t g = g0 + i * stride;
+      if (g < groups) {
+        d[i] = __ldcs(reinterpret_cast<const uint4*>(fp4) + g);
+        sc[i] = __ldcs(reinterpret_cast<const uint16_t*>(s16) + g);
       }
-      e = max(-127, min(127, e));
-      byte = static_cast<uint32_t>(e + 127);
-      // |s| / 2^e: e is in [-13, 9] for any finite non-zero group, so the
-      // power of two is a normal float.
-      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      uint32_t l0, h0, l1, h1;
-      build_lut(a0 * inv, l0, h0);
-      build_lut(a1 * inv, l1, h1);
-      const uint32_t sx0 = (sb0 & 0x80u) ? 0x88888888u : 0u;
-      const uint32_t sx1 = (sb1 & 0x80u) ? 0x88888888u : 0u;
-      o.x = remap8(d.x, l0, h0, sx0);
-      o.y = remap8(d.y, l0, h0, sx0);
-      o.z = remap8(d.z, l1, h1, sx1);
-      o.w = remap8(d.w, l1, h1, sx1);
     }
-    __stcs(reinterpret_cast<uint4*>(out) + g, o);
-    s32[g] = static_cast<uint8_t>(byte);
+#pragma unroll
+    for (int i = 0; i < kRqUnroll; ++i) {
+      const int64_t g = g0 + i * stride;
+      if (g < groups) {
+        uint4 o;
+        uint32_t byte;
+        requant_group(d[i], sc[i], o, byte, err);
+        __stcs(reinterpret_cast<uint4*>(out) + g, o);
+        s32[g] = static_cast<uint8_t>(byte);
+      }
+    }
   }
 }
 
@@ -602,7 +625,7 @@ cudaError_t launch_requant(const uint8_t* fp4, const uint8_t* s16,
                            uint8_t* s32_out, int* err, cudaStream_t st) {
   const int64_t groups = rows * (K / 32);
   if (groups == 0) return cudaSuccess;
-  const int64_t want = (groups + 255) / 256;
+  const int64_t want = (groups + 256 * kRqUnroll - 1) / (256 * kRqUnroll);
   const int blocks = static_cast<int>(std::min<int64_t>(want, num_sms() * 8));
   requant_kernel<<<blocks, 256, 0, st>>>(fp4, s16, groups, fp4_out, s32_out,
                                          err);

@@ -60,6 +60,7 @@ class _OrcMoe(ctypes.Structure):
         ("x_bf16", ctypes.c_void_p), ("xq", ctypes.c_void_p),
         ("xs", ctypes.c_void_p), ("logits", ctypes.c_void_p),
         ("T", ctypes.c_int64), ("h_out", ctypes.c_void_p),
+        ("aux_out", ctypes.c_void_p),
     ]
 
 
@@ -233,7 +234,8 @@ def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
              xs=None, nthreads=None, return_h=False):
     """MoE output rows y[t] in FP64 (before the final bf16 rounding), S2-S7.
 
-    With return_h, also returns the unrounded intermediate h [ntok, k, I]."""
+    With return_h, also returns the unrounded intermediate h [ntok, k, I]
+    and aux [ntok, k, I, 4] = (G, U, sum|G terms|, sum|U terms|)."""
     E, twoI, kb = w13.shape
     K, I = kb * 2, twoI // 2
     T = logits.shape[0]
@@ -253,13 +255,15 @@ def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
         arrs["xs"] = np.ascontiguousarray(xs, dtype=np.uint8)
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
     h = np.empty((tok.size, top_k, I), dtype=np.float64) if return_h else None
+    aux = (np.empty((tok.size, top_k, I, 4), dtype=np.float64) if return_h
+           else None)
     args = _OrcMoe(
         _ptr(arrs["w13"]), _ptr(arrs["w13_s"]), _ptr(arrs["w13_gs"]),
         _ptr(arrs["w2"]), _ptr(arrs["w2_s"]), _ptr(arrs["w2_gs"]),
         E, K, I, gran, w13_layout, act_mode, top_k, nthreads or cores(),
         _ptr(arrs["x_bf16"]), _ptr(arrs["xq"]), _ptr(arrs["xs"]),
-        _ptr(arrs["logits"]), T, _ptr(h))
+        _ptr(arrs["logits"]), T, _ptr(h), _ptr(aux))
     y = np.empty((tok.size, K), dtype=np.float64)
     if lib().orc_moe_rows(ctypes.byref(args), _ptr(tok), tok.size, _ptr(y)):
         raise ValueError("oracle moe_rows rejected its input")
-    return (y, h) if return_h else y
+    return (y, h, aux) if return_h else y

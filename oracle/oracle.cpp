@@ -324,7 +324,8 @@ int orc_act_quant(const uint16_t* x, int64_t T, int64_t K, uint8_t* q,
 //   o_n = gs2 * sum_i h_i * w2[n, i]
 //   y_t = sum_j w_{t,j} * o_{(t,j)}, in top-k order.  Returned in FP64; the
 //   product rounds y to bfloat16 (orc_bf16_rne gives that rounding).
-//   If h_out is set, the unrounded h of each (token, slot) is stored there.
+//   If h_out is set, the unrounded h of each (token, slot) is stored there;
+//   aux_out receives G, U and the sums of |terms| behind them.
 // act_mode 0 reads x_bf16 [T, K]; act_mode 1 reads xq [T, K] (E4M3) and
 // xs [T, K/32] (UE8M0).
 struct OrcMoe {
@@ -341,6 +342,8 @@ struct OrcMoe {
   const float* logits;
   int64_t T;
   double* h_out;  // optional [ntok, top_k, I]: h before its rounding
+  double* aux_out;  // optional [ntok, top_k, I, 4]: G, U, sum|G terms|,
+                    // sum|U terms| (the scale of FP32 rounding in G and U)
 };
 
 static double weight_value(const uint8_t* w, const uint8_t* s, int gran,
@@ -352,12 +355,17 @@ static double weight_value(const uint8_t* w, const uint8_t* s, int gran,
   return orc_e2m1_value(code) * sc;
 }
 
-// One row dot product: sum_k x[k] * dequant(w[row, k]) (FP64).
+// One row dot product: sum_k x[k] * dequant(w[row, k]) (FP64); *abs_sum
+// (if given) receives sum_k |x[k] * dequant(w[row, k])|.
 static double row_dot(const uint8_t* w, const uint8_t* s, int gran, int64_t Kd,
-                      int64_t row, const double* x) {
-  double acc = 0.0;
-  for (int64_t k = 0; k < Kd; ++k)
-    acc += x[k] * weight_value(w, s, gran, Kd, row, k);
+                      int64_t row, const double* x, double* abs_sum = nullptr) {
+  double acc = 0.0, a = 0.0;
+  for (int64_t k = 0; k < Kd; ++k) {
+    const double t = x[k] * weight_value(w, s, gran, Kd, row, k);
+    acc += t;
+    a += std::fabs(t);
+  }
+  if (abs_sum) *abs_sum = a;
   return acc;
 }
 
@@ -405,7 +413,7 @@ int orc_moe_rows(const OrcMoe* a, const int64_t* tokens, int64_t ntok,
   if (K % a->gran || I % a->gran) return 1;
   if (a->act_mode == 1 && (K % 32 || I % 32)) return 1;
   std::vector<int32_t> ids(a->top_k);
-  std::vector<double> w(a->top_k), x(K), g(I), u(I), h(I), o(K);
+  std::vector<double> w(a->top_k), x(K), g(I), u(I), h(I), o(K), sg(I), su(I);
   for (int64_t n = 0; n < ntok; ++n) {
     int64_t t = tokens[n];
     if (t < 0 || t >= a->T) return 1;
@@ -430,12 +438,21 @@ int orc_moe_rows(const OrcMoe* a, const int64_t* tokens, int64_t ntok,
       const int64_t up0 = (a->w13_layout == 0) ? I : 0;
       const double gs13 = a->w13_gs[e], gs2 = a->w2_gs[e];
       parallel_for(I, a->nthreads, [&](int64_t i) {
-        g[i] = gs13 * row_dot(w13, w13s, a->gran, K, gate0 + i, x.data());
-        u[i] = gs13 * row_dot(w13, w13s, a->gran, K, up0 + i, x.data());
+        g[i] = gs13 * row_dot(w13, w13s, a->gran, K, gate0 + i, x.data(), &sg[i]);
+        u[i] = gs13 * row_dot(w13, w13s, a->gran, K, up0 + i, x.data(), &su[i]);
         h[i] = g[i] / (1.0 + std::exp(-g[i])) * u[i];
       });
       if (a->h_out)
         std::copy(h.begin(), h.end(), a->h_out + (n * a->top_k + j) * I);
+      if (a->aux_out) {
+        double* ax = a->aux_out + (n * a->top_k + j) * I * 4;
+        for (int64_t i = 0; i < I; ++i) {
+          ax[4 * i] = g[i];
+          ax[4 * i + 1] = u[i];
+          ax[4 * i + 2] = std::fabs(gs13) * sg[i];
+          ax[4 * i + 3] = std::fabs(gs13) * su[i];
+        }
+      }
       round_intermediate(h, a->act_mode);
       parallel_for(K, a->nthreads, [&](int64_t c) {
         o[c] = gs2 * row_dot(w2, w2s, a->gran, I, c, h.data());

@@ -69,19 +69,19 @@ def check_against_oracle(orc, cfg, w, acts, p, y, ws, tokens, layout=0,
     if cfg.act == "fp8":
         w_used = requant_weights_oracle(orc, w, cfg.E, cfg.K, cfg.I)
         xq, xs = orc.act_quant(acts["x_bf16"])
-        ref_y, ref_h = orc.moe_rows(tokens, **w_used, gran=32,
+        ref_y, ref_h, aux = orc.moe_rows(tokens, **w_used, gran=32,
                                     w13_layout=layout, act_mode=1,
                                     top_k=cfg.top_k, logits=acts["logits"],
                                     xq=xq, xs=xs, return_h=True)
         gran, act = 32, 1
     else:
         w_used, act = w, 0
-        ref_y, ref_h = orc.moe_rows(tokens, **w, gran=gran,
+        ref_y, ref_h, aux = orc.moe_rows(tokens, **w, gran=gran,
                                     w13_layout=layout, act_mode=0,
                                     top_k=cfg.top_k, logits=acts["logits"],
                                     x_bf16=acts["x_bf16"], return_h=True)
-    return check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, w_used,
-                     gran, act, acts["logits"], what or cfg.name)
+    return check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, aux,
+                     w_used, gran, act, acts["logits"], what or cfg.name)
 
 
 # ------------------------------------------------------------------ layout
