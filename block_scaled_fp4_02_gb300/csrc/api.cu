@@ -23,18 +23,20 @@ struct fp4moe_packed {
 // Per-device status word: kernels record the first data-dependent error.
 __device__ int g_fp4moe_status;
 
+namespace fp4moe {
+int* status_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fp4moe_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+}  // namespace fp4moe
+
 namespace {
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
-
-int* status_word() {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_fp4moe_status) != cudaSuccess) return nullptr;
-  return static_cast<int*>(p);
-}
 
 int sm_count() {
   static std::mutex mu;

@@ -91,4 +91,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
 // Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
 int gemm_chunk_max(int T);
 
+// Device address of the per-device status word (kernels record errors there).
+int* status_word();
+
 }  // namespace fp4moe

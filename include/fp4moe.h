@@ -199,6 +199,33 @@ int fp4moe_route_debug(const float* logits, int T, int E, int top_k,
 #define FP4MOE_STAGE_EVENTS 8
 int fp4moe_set_stage_events(void* const* events, int n);
 
+/* Allocation-free routing + permutation, for callers that cannot allocate
+ * device memory where they route tokens: for example a plugin inside a
+ * framework whose own allocator owns the device memory pool, or a
+ * latency-critical loop where cudaMalloc could synchronise the device.  The
+ * pages have no counterpart: this is a library convenience.
+ * It computes exactly what fp4moe_route_debug computes (same outputs, same
+ * argument rules) but takes no workspace: its scratch lives in one array of
+ * FP4MOE_NOALLOC_SCRATCH_BYTES in device global memory that the library
+ * owns, which every GPU that loads the library keeps until the process exits.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up that array's device address (once
+ *     per device, with the device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, and each call overwrites what it uses,
+ *     so calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ *   - Sizes whose scratch (fp4moe_route_noalloc_scratch_bytes) exceeds the
+ *     array return FP4MOE_ERR_WORKSPACE_TOO_SMALL before launching anything;
+ *     the scratch is about 8 * ceil(T/32) * E bytes, so 4 MiB covers, e.g.,
+ *     T = 8192 tokens with E = 1024 experts or T = 32768 with E = 256. */
+#define FP4MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+size_t fp4moe_route_noalloc_scratch_bytes(int T, int E);
+int fp4moe_route_noalloc(const float* logits, int T, int E, int top_k,
+                         int32_t* ids, float* w, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv,
+                         void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* fp4moe_status_string(int status);
 
