@@ -53,8 +53,9 @@ enum fp4moe_act_mode { FP4MOE_ACT_BF16 = 0, FP4MOE_ACT_FP8 = 1 };
 
 /* Flag OR-ed into act_mode of fp4moe_prepare_weights: refuse the lossy
  * group16 -> group32 requant that the FP8 path otherwise runs, mirroring the
- * capability gate of the group16 notes page ("layout-supported but
- * fused-compute unsupported"): FP8 + gran_k 16 + this flag -> UNSUPPORTED. */
+ * capability gate of the group16 notes page (group16 scales are accepted by
+ * the layout transform but not by the fused FP8 compute):
+ * FP8 + gran_k 16 + this flag -> UNSUPPORTED. */
 #define FP4MOE_FLAG_NO_REQUANT 0x100
 
 /* Opaque prepared weights.  Owned by the library until fp4moe_free_packed. */

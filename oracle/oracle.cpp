@@ -7,9 +7,9 @@
 // Sources (page title, then section):
 //  * "DeepGEMM commits, branch cch/deepgemm-glm52-nvfp4-group16" -- the
 //    requant commit: group16 -> group32 recomputes UE8M0 scales.
-//  * "glm52_nvfp4_group16_notes.md", section "Requantization path":
-//    dequantize with the original group16 scales, requantize with group32
-//    scales; lossy, not a metadata rewrite.
+//  * "glm52_nvfp4_group16_notes.md", section "Requantization path": the
+//    group16 values are restored with their own scales and re-encoded with
+//    one new scale per 32 values, which changes the codes (a lossy step).
 //  * "b12x/moe/fused/w4a16/prepare.py": E2M1 packing (two codes per byte, low
 //    nibble = even k), NVFP4 E4M3 scales per 16, per-tensor FP32 global scale,
 //    E8M0 scales per 32, and the gate/up order of the fused FC1 weight
