@@ -13,9 +13,13 @@
 //                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16);
 //   warp 2      : activation producer -- TMA of the token rows of each K step
 //                 into the B half of a ring of A/B stages;
-//   warps 3..10 : dequantizers (warp w owns rows 32*(w%4).. and one 32-wide
-//                 K half of each step), writing the A half of the A/B stage;
-//   warps 11..14: epilogue, reading one of two TMEM accumulators while the
+//   warps 3..18 : dequantizers in two groups of eight that take alternate K
+//                 steps (within a group, warp w owns rows 32*(w%4).. and one
+//                 32-wide K half of the step), writing the A half of the A/B
+//                 stage -- two steps are in flight, so the latency of one
+//                 step's chain (barrier waits, shared-memory round trips,
+//                 proxy fence) overlaps the other;
+//   warps 19..22: epilogue, reading one of two TMEM accumulators while the
 //                 MMA fills the other.
 // The weight ring runs ahead of the A/B ring, so weight bytes in flight are
 // bounded by the F ring depth, not by the (larger) operand stages.  All waits
@@ -28,26 +32,44 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kWarps = 15;
-constexpr int kThreads = kWarps * 32;
-constexpr int kDqWarps = 8;
+constexpr int kDqGroups = 2;     // dequant groups, alternate K steps
+constexpr int kDqWarps = 8;      // warps per dequant group
 constexpr int kEpiWarps = 4;
 constexpr int kWarpFProd = 0, kWarpMma = 1, kWarpBProd = 2, kWarpDq0 = 3,
-              kWarpEpi0 = 11;
+              kWarpEpi0 = kWarpDq0 + kDqGroups * kDqWarps,
+              kWarpMma2 = kWarpEpi0 + kEpiWarps;
+constexpr int kWarps = kWarpMma2 + 1;
+constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kABytes = kTileN * kTileK * 2;  // 16 KB bf16 tile
 constexpr uint32_t kFBytes = 4608;                 // >= largest packed tile
 constexpr uint32_t kTmemCols = 512;                // two 256-column buffers
 
 template <int NT>
 struct Cfg {
+  // With few tokens per unit (decode), each MMA is short and reading the
+  // 128-row A operand from shared memory dominates its cost, so the
+  // dequantized A stages live in TMEM (columns 256..511) instead.
+  static constexpr bool kATmem = NT <= 64;
+  static constexpr uint32_t kASmem = kATmem ? 0 : kABytes;
   static constexpr uint32_t kBBytes = NT * 128;  // NT rows x 64 bf16
-  static constexpr uint32_t kABStage = kABytes + kBBytes;
-  static constexpr int kSA = NT >= 256 ? 4 : 3;
-  static constexpr int kSF = NT >= 256 ? 6 : 32;
+  static constexpr uint32_t kABStage = kASmem + kBBytes;
+  static constexpr uint32_t kATmemCol = 256;     // first TMEM column of A
+  // Each MMA costs a fixed ~90 cycles to issue when N is small, so with few
+  // tokens two warps issue MMAs, taking alternate K steps (the same split as
+  // the dequant groups) into their own accumulators, summed in the epilogue.
+  static constexpr int kMmaWarps = kATmem ? 2 : 1;
+  static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 256;  // per buffer
+  // Stage counts are multiples of kDqGroups, so a dequant group always
+  // meets the same stages.
+  static constexpr int kSA = kATmem ? 8 : 4;   // A stages: 8 x 32 TMEM cols
+  static constexpr int kSF = kATmem ? 30 : 4;
   static constexpr uint32_t kFOff = kABStage * kSA;
   static constexpr uint32_t kBarOff = kFOff + kFBytes * kSF;
   static constexpr int kNumBars = 2 * kSF + 3 * kSA + 5;
-  static constexpr uint32_t kSmem = kBarOff + 8 * kNumBars + 16 + 1024;
+  // cstart[0..E] and offsets[0..E] copied to shared memory for the per-unit
+  // lookups of every role.
+  static constexpr uint32_t kTabOff = kBarOff + 8 * kNumBars + 16;
+  static constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
 };
 
 struct Unit {
@@ -55,16 +77,18 @@ struct Unit {
 };
 
 // Units are ordered (expert, weight block, token chunk); expert e owns
-// nblocks * (cstart[e+1] - cstart[e]) consecutive units.
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
+// nblocks * (cstart[e+1] - cstart[e]) consecutive units.  cs/os are the
+// shared-memory copies of cstart and offsets.
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cs_,
+                                            const int* os, int u) {
   int lo = 0, hi = a.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (a.nblocks * __ldg(a.cstart + mid) <= u) lo = mid; else hi = mid;
+    if (a.nblocks * cs_[mid] <= u) lo = mid; else hi = mid;
   }
-  const int c0 = __ldg(a.cstart + lo), nch = __ldg(a.cstart + lo + 1) - c0;
+  const int c0 = cs_[lo], nch = cs_[lo + 1] - c0;
   const int local = u - a.nblocks * c0;
-  const int o0 = __ldg(a.offsets + lo), cnt = __ldg(a.offsets + lo + 1) - o0;
+  const int o0 = os[lo], cnt = os[lo + 1] - o0;
   const int cs = (cnt + nch - 1) / nch;
   const int c = local % nch;
   Unit U;
@@ -116,6 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto accEmpty = [&](int b) { return bars + 8u * (2 * SF + 3 * SA + 2 + b); };
   const uint32_t done_bar = bars + 8u * (2 * SF + 3 * SA + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 8 * C::kNumBars);
+  int* tab_cs = reinterpret_cast<int*>(smem + C::kTabOff);
+  int* tab_os = tab_cs + (kMaxE + 1);
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+    tab_cs[i] = __ldg(a.cstart + i);
+    tab_os[i] = __ldg(a.offsets + i);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SF; ++s) {
@@ -128,10 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(emptyAB(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accFull(b), 1);
+      mbar_init(accFull(b), C::kMmaWarps);
       mbar_init(accEmpty(b), kEpiWarps);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, C::kMmaWarps);
     fence_barrier_init();
   }
   if (warp == kWarpBProd && lane == 0) prefetch_tensormap(&tmB);
@@ -143,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = a.nblocks * __ldg(a.cstart + a.E);
+  const int total = a.nblocks * tab_cs[a.E];
 
   if (warp == kWarpFProd) {
     // ------------------------------------------------- weight producer
@@ -152,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, u);
+        const Unit U = decode_unit(a, tab_cs, tab_os, u);
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
         for (int ks = 0; ks < a.ksteps; ++ks) {
@@ -177,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, u);
+        const Unit U = decode_unit(a, tab_cs, tab_os, u);
         const int nbox = (U.ntok + 15) >> 4;
         for (int ks = 0; ks < a.ksteps; ++ks) {
           if (!mbar_wait(emptyAB(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(fullB(s), nbox * 2048u);
-          const uint32_t dst = sbase + s * C::kABStage + kABytes;
+          const uint32_t dst = sbase + s * C::kABStage + C::kASmem;
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(dst + b * 2048u, &tmB, ks * kTileK, U.row0 + 16 * b, fullB(s));
           issued |= 1u << s;
@@ -194,30 +224,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < SA; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int s = 0, buf = 0;
-      uint32_t ph = 0, acc_ph = 0;
+    const int mi = (warp == kWarpMma) ? 0 : 1;   // takes K steps n % kMmaWarps == mi
+    if (mi < C::kMmaWarps && lane == 0) {
+      int buf = 0;
+      uint32_t n = 0, acc_ph = 0;
       bool ok = true;
+      const uint64_t adesc0 = sw128_kmajor_desc(sbase);
+      const uint64_t bdesc0 = sw128_kmajor_desc(sbase + C::kASmem);
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, u);
-        const uint32_t n = static_cast<uint32_t>((U.ntok + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(128, n);
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * 256u;
+        const Unit U = decode_unit(a, tab_cs, tab_os, u);
+        const uint32_t nn = static_cast<uint32_t>((U.ntok + 15) & ~15);
+        const uint32_t idesc = idesc_bf16_f32(128, nn);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * C::kAccCols +
+                                static_cast<uint32_t>(mi * NT);
         if (!mbar_wait(accEmpty(buf), acc_ph ^ 1u)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < a.ksteps; ++ks) {
+        uint32_t acc = 0;
+        for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
+          if (static_cast<int>(n % C::kMmaWarps) != mi) continue;
+          const int s = static_cast<int>(n % SA);
+          const uint32_t ph = (n / SA) & 1u;
           if (!mbar_wait(fullB(s), ph) || !mbar_wait(aready(s), ph)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = sbase + s * C::kABStage;
+          // Descriptors advance by the stage offset and 32 B per K=16 step
+          // (2 in the descriptor's 16-byte address units).
+          const uint64_t so = static_cast<uint64_t>((s * C::kABStage) >> 4);
+          const uint64_t bd = bdesc0 + so;
+          if (C::kATmem) {
+            const uint32_t at = tmem + C::kATmemCol + s * 32u;
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk)
-            umma_f16(d_tmem, sw128_kmajor_desc(st + kk * 32),
-                     sw128_kmajor_desc(st + kABytes + kk * 32), idesc,
-                     (ks | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              umma_f16_ta(d_tmem, at + kk * 8u, bd + 2u * kk, idesc, acc);
+              acc = 1u;
+            }
+          } else {
+            const uint64_t ad = adesc0 + so;
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              umma_f16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+              acc = 1u;
+            }
+          }
           umma_commit(emptyAB(s));
-          if (++s == SA) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         umma_commit(accFull(buf));
@@ -230,18 +280,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpEpi0) {
     // ---------------------------------------------------------- dequant
-    const int dq = warp - kWarpDq0;   // 0..7
-    const int q = warp & 3;           // row quarter
-    const int khalf = dq >> 2;        // 32-wide K half of each step
+    const int dq = warp - kWarpDq0;   // 0 .. kDqGroups*8-1
+    const int grp = dq / kDqWarps;    // takes K steps n with n % kDqGroups == grp
+    const int w8 = dq % kDqWarps;
+    const int q = warp & 3;           // row quarter = TMEM lane quarter
+    const int khalf = w8 >> 2;        // 32-wide K half of each step
     const int r = 32 * q + lane;      // weight row in the tile
     const uint32_t smul = a.smul, sadd = a.sadd;
     const uint32_t a_row_off = (r >> 3) * 1024u + (r & 7) * 128u;
     const uint32_t sw = r & 7, cb = 4 * khalf;
-    int sf = 0, sa = 0;
-    uint32_t phf = 0, pha = 0;
+    uint32_t n = 0;                   // global K-step counter of this CTA
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      for (int ks = 0; ks < a.ksteps; ++ks) {
+      for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
+        if (static_cast<int>(n % kDqGroups) != grp) continue;
+        const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SA);
+        const uint32_t phf = (n / SF) & 1u, pha = (n / SA) & 1u;
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
         const uint8_t* f = smem + C::kFOff + sf * kFBytes;
         const uint4 d = *reinterpret_cast<const uint4*>(f + khalf * 2048 + r * 16);
@@ -256,22 +310,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(emptyF(sf));
-        if (++sf == SF) { sf = 0; phf ^= 1u; }
         uint32_t s0 = c0 * smul + sadd, s1 = c1 * smul + sadd;
         s0 |= s0 << 16;
         s1 |= s1 << 16;
         const uint4 w0 = dequant8(d.x, s0), w1 = dequant8(d.y, s0);
         const uint4 w2 = dequant8(d.z, s1), w3 = dequant8(d.w, s1);
         if (!mbar_wait(emptyAB(sa), pha ^ 1u)) { ok = false; break; }
-        const uint32_t arow = sbase + sa * C::kABStage + a_row_off;
-        st_shared_v4(arow + (((cb + 0) ^ sw) << 4), w0);
-        st_shared_v4(arow + (((cb + 1) ^ sw) << 4), w1);
-        st_shared_v4(arow + (((cb + 2) ^ sw) << 4), w2);
-        st_shared_v4(arow + (((cb + 3) ^ sw) << 4), w3);
-        fence_proxy_async_smem();
+        if (C::kATmem) {
+          tc_fence_after();   // after the MMA that last read this stage
+          // Row r of A -> TMEM lane r; this K half -> 16 columns.
+          const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                  w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+          tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
+                        sa * 32u + khalf * 16u, v);
+          tmem_st_wait();
+          tc_fence_before();
+        } else {
+          const uint32_t arow = sbase + sa * C::kABStage + a_row_off;
+          st_shared_v4(arow + (((cb + 0) ^ sw) << 4), w0);
+          st_shared_v4(arow + (((cb + 1) ^ sw) << 4), w1);
+          st_shared_v4(arow + (((cb + 2) ^ sw) << 4), w2);
+          st_shared_v4(arow + (((cb + 3) ^ sw) << 4), w3);
+          fence_proxy_async_smem();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(aready(sa));
-        if (++sa == SA) { sa = 0; pha ^= 1u; }
       }
     }
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
@@ -283,16 +346,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit U = decode_unit(a, u);
+      const Unit U = decode_unit(a, tab_cs, tab_os, u);
       if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
       const int nchunks = (U.ntok + 15) >> 4;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                              static_cast<uint32_t>(buf) * 256u;
+                              static_cast<uint32_t>(buf) * C::kAccCols;
       for (int j = 0; j < nchunks; ++j) {
         uint32_t v[16];
         tmem_ld16(t_base + 16 * j, v);
+        if (C::kMmaWarps > 1) {
+          uint32_t w[16];
+          tmem_ld16(t_base + static_cast<uint32_t>(NT) + 16 * j, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
+        }
         tmem_ld_wait();
         if (MODE == kGemmModeFc2) {
           float* o = static_cast<float*>(a.out);
