@@ -2,29 +2,31 @@
 // (sm_103a, tcgen05): FC1 gate|up with the SwiGLU epilogue and FC2.
 //
 // Formulation (weights as the UMMA M side): for each work unit (expert e,
-// 128-row weight block nb, chunk of up to NT tokens of e),
-//     D[128 x n] = W_tile[128 x Kd] * X_chunk[n x Kd]^T    (FP32 in TMEM)
-// W is dequantized FP4 -> bf16 into shared memory in the 128-byte swizzled
+// MT consecutive 128-row weight blocks, chunk of up to NT tokens of e),
+//     D_t[128 x n] = W_tile_t[128 x Kd] * X_chunk[n x Kd]^T   (FP32, TMEM)
+// W is dequantized FP4 -> bf16 into shared memory (or TMEM) in the UMMA
 // K-major layout; X (bf16 activations in expert-major order) arrives by TMA
-// in the same layout.  Warp roles, one CTA per SM, persistent over units:
+// in the 128-byte swizzled layout.  Two variants:
+//   NT = 256 (many tokens per expert): MT = 2 weight tiles share each
+//     activation tile, which halves activation traffic per MMA; A in shared
+//     memory; two accumulators of 256 columns fill TMEM.
+//   NT = 64 (decode): MT = 1; each MMA is short and costs a fixed ~90 cycles
+//     to issue, so A lives in TMEM and two MMA warps take alternate K steps
+//     into their own accumulators (summed in the epilogue), double-buffered.
+// Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
-//                 (one per 64-wide K step) into a deep ring of F stages;
-//   warp 1      : TMEM allocation and the single UMMA-issuing thread
+//                 (MT per 64-wide K step) into a ring of F stages;
+//   warp 1 (+27): TMEM allocation and the UMMA-issuing thread(s)
 //                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16);
 //   warp 2      : activation producer -- TMA of the token rows of each K step
-//                 into the B half of a ring of A/B stages;
-//   warps 3..18 : dequantizers in two groups of eight that take alternate K
-//                 steps (within a group, warp w owns rows 32*(w%4).. and one
-//                 32-wide K half of the step), writing the A half of the A/B
-//                 stage -- two steps are in flight, so the latency of one
-//                 step's chain (barrier waits, shared-memory round trips,
-//                 proxy fence) overlaps the other;
-//   warps 19..22: epilogue, reading one of two TMEM accumulators while the
-//                 MMA fills the other.
-// The weight ring runs ahead of the A/B ring, so weight bytes in flight are
-// bounded by the F ring depth, not by the (larger) operand stages.  All waits
-// are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in the device
-// status word and the CTA winds down and frees its TMEM.
+//                 into the B part of a ring of A/B stages;
+//   warps 3..18 : dequantizers in two groups of eight (within a group, warp w
+//                 owns rows 32*(w%4).. and one 32-wide K half of the step):
+//                 with MT = 2 group g fills weight tile g of every step, with
+//                 MT = 1 the groups take alternate steps;
+//   warps 19..26: epilogue, reading the TMEM accumulators.
+// All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
+// the device status word and the CTA winds down and frees its TMEM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,9 +34,9 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kDqGroups = 2;     // dequant groups, alternate K steps
+constexpr int kDqGroups = 2;     // dequant groups
 constexpr int kDqWarps = 8;      // warps per dequant group
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;
 constexpr int kWarpFProd = 0, kWarpMma = 1, kWarpBProd = 2, kWarpDq0 = 3,
               kWarpEpi0 = kWarpDq0 + kDqGroups * kDqWarps,
               kWarpMma2 = kWarpEpi0 + kEpiWarps;
@@ -42,58 +44,65 @@ constexpr int kWarps = kWarpMma2 + 1;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kABytes = kTileN * kTileK * 2;  // 16 KB bf16 tile
 constexpr uint32_t kFBytes = 4608;                 // >= largest packed tile
-constexpr uint32_t kTmemCols = 512;                // two 256-column buffers
+constexpr uint32_t kTmemCols = 512;
 
 template <int NT>
 struct Cfg {
-  // With few tokens per unit (decode), each MMA is short and reading the
-  // 128-row A operand from shared memory dominates its cost, so the
-  // dequantized A stages live in TMEM (columns 256..511) instead.
-  static constexpr bool kATmem = NT <= 64;
-  static constexpr uint32_t kASmem = kATmem ? 0 : kABytes;
-  static constexpr uint32_t kBBytes = NT * 128;  // NT rows x 64 bf16
-  static constexpr uint32_t kABStage = kASmem + kBBytes;
-  static constexpr uint32_t kATmemCol = 256;     // first TMEM column of A
-  // Each MMA costs a fixed ~90 cycles to issue when N is small, so with few
-  // tokens two warps issue MMAs, taking alternate K steps (the same split as
-  // the dequant groups) into their own accumulators, summed in the epilogue.
+  static constexpr bool kATmem = NT <= 64;         // A stages in TMEM
+  static constexpr int kMT = kATmem ? 1 : 2;       // weight tiles per unit
   static constexpr int kMmaWarps = kATmem ? 2 : 1;
-  static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 256;  // per buffer
-  // Stage counts are multiples of kDqGroups, so a dequant group always
-  // meets the same stages.
-  static constexpr int kSA = kATmem ? 8 : 4;   // A stages: 8 x 32 TMEM cols
-  static constexpr int kSF = kATmem ? 30 : 4;
-  static constexpr uint32_t kFOff = kABStage * kSA;
-  static constexpr uint32_t kBarOff = kFOff + kFBytes * kSF;
-  static constexpr int kNumBars = 2 * kSF + 3 * kSA + 5;
+  // Rings: F (packed weights, from HBM), A (dequantized weights, shared
+  // memory or TMEM), B (activation rows, from L2 by TMA).
+  static constexpr int kSF = kATmem ? 24 : 6;
+  static constexpr int kSAa = kATmem ? 8 : 2;      // NT=64: 8 x 32 TMEM cols
+  static constexpr int kSB = kATmem ? 8 : 3;
+  static constexpr uint32_t kFStage = kFBytes * kMT;
+  static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
+  static constexpr uint32_t kBStage = NT * 128;    // NT rows x 64 bf16
+  static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
+  static constexpr int kAccBufs = kATmem ? 2 : 1;
+  static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
+  static constexpr int kDqPerStage = kATmem ? kDqWarps : kDqGroups * kDqWarps;
+  static constexpr uint32_t kAOff = 0;
+  static constexpr uint32_t kBOff = kAOff + kAStage * kSAa;
+  static constexpr uint32_t kFOff = kBOff + kBStage * kSB;
+  static constexpr uint32_t kBarOff = kFOff + kFStage * kSF;
+  static constexpr int kNumBars = 2 * kSF + 2 * kSAa + 2 * kSB + 2 * kAccBufs + 1;
   // cstart[0..E] and offsets[0..E] copied to shared memory for the per-unit
   // lookups of every role.
   static constexpr uint32_t kTabOff = kBarOff + 8 * kNumBars + 16;
   static constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
+                          kATmemCol + 32 * kSAa <= kTmemCols)
+                       : kAccCols <= kTmemCols, "TMEM budget");
+  static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
+                "swizzled operands need 1 KB alignment");
 };
 
 struct Unit {
-  int e, nb, row0, ntok;
+  int e, nb, row0, ntok;   // nb: first 128-row weight block of the unit
 };
 
-// Units are ordered (expert, weight block, token chunk); expert e owns
-// nblocks * (cstart[e+1] - cstart[e]) consecutive units.  cs/os are the
-// shared-memory copies of cstart and offsets.
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cs_,
+// Units are ordered (expert, weight-block group, token chunk); expert e owns
+// nbu * (cstart[e+1] - cstart[e]) consecutive units, nbu = ceil(nblocks/MT).
+// cs_/os are the shared-memory copies of cstart and offsets.
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
+                                            int mt, const int* cs_,
                                             const int* os, int u) {
   int lo = 0, hi = a.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (a.nblocks * cs_[mid] <= u) lo = mid; else hi = mid;
+    if (nbu * cs_[mid] <= u) lo = mid; else hi = mid;
   }
   const int c0 = cs_[lo], nch = cs_[lo + 1] - c0;
-  const int local = u - a.nblocks * c0;
+  const int local = u - nbu * c0;
   const int o0 = os[lo], cnt = os[lo + 1] - o0;
   const int cs = (cnt + nch - 1) / nch;
   const int c = local % nch;
   Unit U;
   U.e = lo;
-  U.nb = local / nch;
+  U.nb = (local / nch) * mt;
   U.row0 = o0 + c * cs;
   U.ntok = min(cs, cnt - c * cs);
   return U;
@@ -124,7 +133,7 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
   using C = Cfg<NT>;
-  constexpr int SA = C::kSA, SF = C::kSF;
+  constexpr int SF = C::kSF, SAa = C::kSAa, SB = C::kSB, MT = C::kMT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -133,12 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + C::kBarOff;
   auto fullF = [&](int s) { return bars + 8u * s; };
   auto emptyF = [&](int s) { return bars + 8u * (SF + s); };
-  auto fullB = [&](int s) { return bars + 8u * (2 * SF + s); };
-  auto aready = [&](int s) { return bars + 8u * (2 * SF + SA + s); };
-  auto emptyAB = [&](int s) { return bars + 8u * (2 * SF + 2 * SA + s); };
-  auto accFull = [&](int b) { return bars + 8u * (2 * SF + 3 * SA + b); };
-  auto accEmpty = [&](int b) { return bars + 8u * (2 * SF + 3 * SA + 2 + b); };
-  const uint32_t done_bar = bars + 8u * (2 * SF + 3 * SA + 4);
+  auto aready = [&](int s) { return bars + 8u * (2 * SF + s); };
+  auto emptyA = [&](int s) { return bars + 8u * (2 * SF + SAa + s); };
+  auto fullB = [&](int s) { return bars + 8u * (2 * SF + 2 * SAa + s); };
+  auto emptyB = [&](int s) { return bars + 8u * (2 * SF + 2 * SAa + SB + s); };
+  constexpr int kAccBar0 = 2 * SF + 2 * SAa + 2 * SB;
+  auto accFull = [&](int b) { return bars + 8u * (kAccBar0 + b); };
+  auto accEmpty = [&](int b) { return bars + 8u * (kAccBar0 + C::kAccBufs + b); };
+  const uint32_t done_bar = bars + 8u * (kAccBar0 + 2 * C::kAccBufs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 8 * C::kNumBars);
   int* tab_cs = reinterpret_cast<int*>(smem + C::kTabOff);
   int* tab_os = tab_cs + (kMaxE + 1);
@@ -146,18 +157,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tab_cs[i] = __ldg(a.cstart + i);
     tab_os[i] = __ldg(a.offsets + i);
   }
+  const int nbu = (a.nblocks + MT - 1) / MT;   // weight-block groups per chunk
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SF; ++s) {
       mbar_init(fullF(s), 1);
-      mbar_init(emptyF(s), kDqWarps);
+      mbar_init(emptyF(s), C::kDqPerStage);
     }
-    for (int s = 0; s < SA; ++s) {
+    for (int s = 0; s < SAa; ++s) {
+      mbar_init(aready(s), C::kDqPerStage);
+      mbar_init(emptyA(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
       mbar_init(fullB(s), 1);
-      mbar_init(aready(s), kDqWarps);
-      mbar_init(emptyAB(s), 1);
+      mbar_init(emptyB(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(accFull(b), C::kMmaWarps);
       mbar_init(accEmpty(b), kEpiWarps);
     }
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = a.nblocks * tab_cs[a.E];
+  const int total = nbu * tab_cs[a.E];
 
   if (warp == kWarpFProd) {
     // ------------------------------------------------- weight producer
@@ -182,14 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+        const int tiles = min(MT, a.nblocks - U.nb);
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
+        const int64_t tstride = static_cast<int64_t>(a.ksteps) * a.tile_bytes;
         for (int ks = 0; ks < a.ksteps; ++ks) {
           if (!mbar_wait(emptyF(s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(fullF(s), a.tile_bytes);
-          bulk_load(sbase + C::kFOff + s * kFBytes,
-                    wt + static_cast<int64_t>(ks) * a.tile_bytes, a.tile_bytes, fullF(s));
+          mbar_arrive_expect_tx(fullF(s), tiles * a.tile_bytes);
+          for (int t = 0; t < tiles; ++t)
+            bulk_load(sbase + C::kFOff + s * C::kFStage + t * kFBytes,
+                      wt + t * tstride + static_cast<int64_t>(ks) * a.tile_bytes,
+                      a.tile_bytes, fullF(s));
           issued |= 1u << (s & 31);
           issued_ph = (issued_ph & ~(1u << (s & 31))) | (ph << (s & 31));
           if (++s == SF) { s = 0; ph ^= 1u; }
@@ -207,21 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
         const int nbox = (U.ntok + 15) >> 4;
         for (int ks = 0; ks < a.ksteps; ++ks) {
-          if (!mbar_wait(emptyAB(s), ph ^ 1u)) { ok = false; break; }
+          if (!mbar_wait(emptyB(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(fullB(s), nbox * 2048u);
-          const uint32_t dst = sbase + s * C::kABStage + C::kASmem;
+          const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(dst + b * 2048u, &tmB, ks * kTileK, U.row0 + 16 * b, fullB(s));
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
-          if (++s == SA) { s = 0; ph ^= 1u; }
+          if (++s == SB) { s = 0; ph ^= 1u; }
         }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
-      for (int t = 0; t < SA; ++t)
+      for (int t = 0; t < SB; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
     }
   } else if (warp == kWarpMma || warp == kWarpMma2) {
@@ -231,10 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int buf = 0;
       uint32_t n = 0, acc_ph = 0;
       bool ok = true;
-      const uint64_t adesc0 = sw128_kmajor_desc(sbase);
-      const uint64_t bdesc0 = sw128_kmajor_desc(sbase + C::kASmem);
+      const uint64_t adesc0 = sw128_kmajor_desc(sbase + C::kAOff);
+      const uint64_t bdesc0 = sw128_kmajor_desc(sbase + C::kBOff);
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+        const int tiles = min(MT, a.nblocks - U.nb);
         const uint32_t nn = static_cast<uint32_t>((U.ntok + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, nn);
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * C::kAccCols +
@@ -244,34 +264,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc = 0;
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
           if (static_cast<int>(n % C::kMmaWarps) != mi) continue;
-          const int s = static_cast<int>(n % SA);
-          const uint32_t ph = (n / SA) & 1u;
-          if (!mbar_wait(fullB(s), ph) || !mbar_wait(aready(s), ph)) { ok = false; break; }
+          const int sa = static_cast<int>(n % SAa), sb = static_cast<int>(n % SB);
+          if (!mbar_wait(fullB(sb), (n / SB) & 1u) || !mbar_wait(aready(sa), (n / SAa) & 1u)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           // Descriptors advance by the stage offset and 32 B per K=16 step
           // (2 in the descriptor's 16-byte address units).
-          const uint64_t so = static_cast<uint64_t>((s * C::kABStage) >> 4);
-          const uint64_t bd = bdesc0 + so;
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((sb * C::kBStage) >> 4);
           if (C::kATmem) {
-            const uint32_t at = tmem + C::kATmemCol + s * 32u;
+            const uint32_t at = tmem + C::kATmemCol + sa * 32u;
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
               umma_f16_ta(d_tmem, at + kk * 8u, bd + 2u * kk, idesc, acc);
               acc = 1u;
             }
           } else {
-            const uint64_t ad = adesc0 + so;
+            const uint64_t ad = adesc0 + static_cast<uint64_t>((sa * C::kAStage) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
-              umma_f16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+              for (int t = 0; t < tiles; ++t)   // tile t -> accumulator columns 256 t
+                umma_f16(d_tmem + 256u * t, ad + (kABytes >> 4) * t + 2u * kk,
+                         bd + 2u * kk, idesc, acc);
               acc = 1u;
             }
           }
-          umma_commit(emptyAB(s));
+          umma_commit(emptyA(sa));
+          umma_commit(emptyB(sb));
         }
         if (!ok) break;
         umma_commit(accFull(buf));
-        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+        if (++buf == C::kAccBufs) { buf = 0; acc_ph ^= 1u; }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
       // Let every issued MMA finish before TMEM is released.
@@ -280,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpEpi0) {
     // ---------------------------------------------------------- dequant
-    const int dq = warp - kWarpDq0;   // 0 .. kDqGroups*8-1
-    const int grp = dq / kDqWarps;    // takes K steps n with n % kDqGroups == grp
+    const int dq = warp - kWarpDq0;   // 0 .. 15
+    const int grp = dq / kDqWarps;
     const int w8 = dq % kDqWarps;
     const int q = warp & 3;           // row quarter = TMEM lane quarter
     const int khalf = w8 >> 2;        // 32-wide K half of each step
@@ -289,49 +313,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t smul = a.smul, sadd = a.sadd;
     const uint32_t a_row_off = (r >> 3) * 1024u + (r & 7) * 128u;
     const uint32_t sw = r & 7, cb = 4 * khalf;
+    // MT = 2: group g fills weight tile g of every step; MT = 1: the groups
+    // take alternate steps into the single tile.
+    const int tile = (MT > 1) ? grp : 0;
     uint32_t n = 0;                   // global K-step counter of this CTA
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const bool live = (MT == 1) ||
+                        (decode_unit(a, nbu, MT, tab_cs, tab_os, u).nb + tile < a.nblocks);
       for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
-        if (static_cast<int>(n % kDqGroups) != grp) continue;
-        const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SA);
-        const uint32_t phf = (n / SF) & 1u, pha = (n / SA) & 1u;
-        if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        const uint8_t* f = smem + C::kFOff + sf * kFBytes;
-        const uint4 d = *reinterpret_cast<const uint4*>(f + khalf * 2048 + r * 16);
-        uint32_t c0, c1;
-        if (a.gran == 16) {
-          const uint32_t sc =
-              *reinterpret_cast<const uint16_t*>(f + kTileDataBytes + r * 4 + khalf * 2);
-          c0 = sc & 0xFFu;
-          c1 = sc >> 8;
+        if (MT == 1 && static_cast<int>(n % kDqGroups) != grp) continue;
+        const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SAa);
+        const uint32_t phf = (n / SF) & 1u, pha = (n / SAa) & 1u;
+        uint4 w0, w1, w2, w3;
+        if (live) {
+          if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
+          const uint8_t* f = smem + C::kFOff + sf * C::kFStage + tile * kFBytes;
+          const uint4 d = *reinterpret_cast<const uint4*>(f + khalf * 2048 + r * 16);
+          uint32_t c0, c1;
+          if (a.gran == 16) {
+            const uint32_t sc =
+                *reinterpret_cast<const uint16_t*>(f + kTileDataBytes + r * 4 + khalf * 2);
+            c0 = sc & 0xFFu;
+            c1 = sc >> 8;
+          } else {
+            c0 = c1 = f[kTileDataBytes + r * 2 + khalf];
+          }
+          uint32_t s0 = c0 * smul + sadd, s1 = c1 * smul + sadd;
+          s0 |= s0 << 16;
+          s1 |= s1 << 16;
+          w0 = dequant8(d.x, s0); w1 = dequant8(d.y, s0);
+          w2 = dequant8(d.z, s1); w3 = dequant8(d.w, s1);
         } else {
-          c0 = c1 = f[kTileDataBytes + r * 2 + khalf];
+          // No second weight block (odd block count): nothing to load.
+          if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(emptyF(sf));
-        uint32_t s0 = c0 * smul + sadd, s1 = c1 * smul + sadd;
-        s0 |= s0 << 16;
-        s1 |= s1 << 16;
-        const uint4 w0 = dequant8(d.x, s0), w1 = dequant8(d.y, s0);
-        const uint4 w2 = dequant8(d.z, s1), w3 = dequant8(d.w, s1);
-        if (!mbar_wait(emptyAB(sa), pha ^ 1u)) { ok = false; break; }
-        if (C::kATmem) {
-          tc_fence_after();   // after the MMA that last read this stage
-          // Row r of A -> TMEM lane r; this K half -> 16 columns.
-          const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                  w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-          tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
-                        sa * 32u + khalf * 16u, v);
-          tmem_st_wait();
-          tc_fence_before();
-        } else {
-          const uint32_t arow = sbase + sa * C::kABStage + a_row_off;
-          st_shared_v4(arow + (((cb + 0) ^ sw) << 4), w0);
-          st_shared_v4(arow + (((cb + 1) ^ sw) << 4), w1);
-          st_shared_v4(arow + (((cb + 2) ^ sw) << 4), w2);
-          st_shared_v4(arow + (((cb + 3) ^ sw) << 4), w3);
-          fence_proxy_async_smem();
+        if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
+        if (live) {
+          if (C::kATmem) {
+            tc_fence_after();   // after the MMA that last read this stage
+            // Row r of A -> TMEM lane r; this K half -> 16 columns.
+            const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                    w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+            tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
+                          sa * 32u + khalf * 16u, v);
+            tmem_st_wait();
+            tc_fence_before();
+          } else {
+            const uint32_t arow = sbase + C::kAOff + sa * C::kAStage + tile * kABytes + a_row_off;
+            st_shared_v4(arow + (((cb + 0) ^ sw) << 4), w0);
+            st_shared_v4(arow + (((cb + 1) ^ sw) << 4), w1);
+            st_shared_v4(arow + (((cb + 2) ^ sw) << 4), w2);
+            st_shared_v4(arow + (((cb + 3) ^ sw) << 4), w3);
+            fence_proxy_async_smem();
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(aready(sa));
@@ -340,20 +377,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   } else {
     // --------------------------------------------------------- epilogue
+    const int ew = warp - kWarpEpi0;  // 0..7
     const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int part = ew >> 2;         // MT = 2: weight tile; MT = 1: column half
     const int r = 32 * q + lane;      // weight row in the tile
     int buf = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit U = decode_unit(a, tab_cs, tab_os, u);
+      const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
       if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
       const int nchunks = (U.ntok + 15) >> 4;
+      const int nb = U.nb + (MT > 1 ? part : 0);
+      const bool live = nb < a.nblocks;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                              static_cast<uint32_t>(buf) * C::kAccCols;
-      for (int j = 0; j < nchunks; ++j) {
+                              static_cast<uint32_t>(buf) * C::kAccCols +
+                              (MT > 1 ? 256u * part : 0u);
+      const int j0 = (MT > 1) ? 0 : part, jstep = (MT > 1) ? 1 : 2;
+      for (int j = j0; live && j < nchunks; j += jstep) {
         uint32_t v[16];
         tmem_ld16(t_base + 16 * j, v);
         if (C::kMmaWarps > 1) {
@@ -367,17 +410,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (MODE == kGemmModeFc2) {
           float* o = static_cast<float*>(a.out);
-          const int64_t n = static_cast<int64_t>(U.nb) * kTileN + r;
+          const int64_t col_n = static_cast<int64_t>(nb) * kTileN + r;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int col = 16 * j + c;
             if (col < U.ntok)
-              o[static_cast<int64_t>(U.row0 + col) * a.ldo + n] = __uint_as_float(v[c]) * alpha;
+              o[static_cast<int64_t>(U.row0 + col) * a.ldo + col_n] =
+                  __uint_as_float(v[c]) * alpha;
           }
         } else {
           // Lanes 0..15 hold gate rows, 16..31 the up rows of the same 16
           // intermediate columns; one exchange per column pair.
-          const int i = U.nb * 64 + 16 * q + (lane & 15);
+          const int i = nb * 64 + 16 * q + (lane & 15);
           const bool is_gate = lane < 16;
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
@@ -400,13 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accEmpty(buf));
-      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      if (++buf == C::kAccBufs) { buf = 0; acc_ph ^= 1u; }
     }
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   }
 
-  // ---- teardown: the MMA thread has waited (bounded) for its final commit,
-  // so no UMMA is still writing TMEM; free it.
+  // ---- teardown: the MMA threads have waited (bounded) for their final
+  // commits, so no UMMA is still writing TMEM; free it.
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
