@@ -40,22 +40,45 @@ __device__ __forceinline__ float e2m1_mag(uint32_t m) {
   return __uint_as_float(m << 22) * 0x1p126f;
 }
 
-// Largest 3-bit magnitude among the 16 nibbles of two words.
-__device__ __forceinline__ uint32_t max_mag16(uint32_t a, uint32_t b) {
-  uint32_t x = __vmaxu4(a & 0x07070707u, (a >> 4) & 0x07070707u);
-  uint32_t y = __vmaxu4(b & 0x07070707u, (b >> 4) & 0x07070707u);
-  uint32_t m = __vmaxu4(x, y);
-  m = __vmaxu4(m, m >> 16);
-  m = __vmaxu4(m, m >> 8);
-  return m & 0xFFu;
+// Largest 3-bit magnitude among the 16 nibbles of two words, from bit tests
+// that hold for any nibble: bit 2 of (x & x<<1) is "m >= 6", of
+// (x & x<<1 & x<<2) "m == 7", of (x & (x<<1 | x<<2)) "m >= 5"; for nibbles
+// below 4, bit 1 of (x & x<<1) is "m == 3".
+__device__ __forceinline__ uint32_t max_mag16(uint32_t x, uint32_t y) {
+  const uint32_t b2 = 0x44444444u, b1 = 0x22222222u;
+  const uint32_t hx = x & (x << 1), hy = y & (y << 1);
+  const uint32_t any = x | y;
+  uint32_t m;
+  if (any & b2) {
+    const bool c7 = ((hx & (x << 2)) | (hy & (y << 2))) & b2;
+    const bool c6 = (hx | hy) & b2;
+    const bool c5 = ((x & ((x << 1) | (x << 2))) | (y & ((y << 1) | (y << 2)))) & b2;
+    m = c7 ? 7u : c6 ? 6u : c5 ? 5u : 4u;
+  } else {
+    const bool c3 = (hx | hy) & b1;
+    m = c3 ? 3u : (any & b1) ? 2u : (any & 0x11111111u) ? 1u : 0u;
+  }
+  return m;
+}
+
+// Two non-negative f32 -> two E2M1 codes (RNE, saturating), lo in the low
+// nibble.
+__device__ __forceinline__ uint32_t pos_f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Table of new magnitudes for f = |s| / 2^e: byte m of (lo, hi) = new mag m.
 __device__ __forceinline__ void build_lut(float f, uint32_t& lo, uint32_t& hi) {
-  const uint32_t c01 = f32x2_to_e2m1x2(0.0f, 0.5f * f);
-  const uint32_t c23 = f32x2_to_e2m1x2(1.0f * f, 1.5f * f);
-  const uint32_t c45 = f32x2_to_e2m1x2(2.0f * f, 3.0f * f);
-  const uint32_t c67 = f32x2_to_e2m1x2(4.0f * f, 6.0f * f);
+  const uint32_t c01 = pos_f32x2_to_e2m1x2(0.0f, 0.5f * f);
+  const uint32_t c23 = pos_f32x2_to_e2m1x2(1.0f * f, 1.5f * f);
+  const uint32_t c45 = pos_f32x2_to_e2m1x2(2.0f * f, 3.0f * f);
+  const uint32_t c67 = pos_f32x2_to_e2m1x2(4.0f * f, 6.0f * f);
   lo = (c01 & 0x7u) | ((c01 & 0x70u) << 4) | ((c23 & 0x7u) << 16) |
        ((c23 & 0x70u) << 20);
   hi = (c45 & 0x7u) | ((c45 & 0x70u) << 4) | ((c67 & 0x7u) << 16) |
