@@ -395,19 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
                               static_cast<uint32_t>(buf) * C::kAccCols +
                               (MT > 1 ? 256u * part : 0u);
-      const int j0 = (MT > 1) ? 0 : part, jstep = (MT > 1) ? 1 : 2;
-      for (int j = j0; live && j < nchunks; j += jstep) {
-        uint32_t v[16];
-        tmem_ld16(t_base + 16 * j, v);
-        if (C::kMmaWarps > 1) {
-          uint32_t w[16];
-          tmem_ld16(t_base + static_cast<uint32_t>(NT) + 16 * j, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
-        }
-        tmem_ld_wait();
+      // Stores one 16-column chunk j of accumulator values v.
+      auto emit16 = [&](const uint32_t (&v)[16], int j) {
         if (MODE == kGemmModeFc2) {
           float* o = static_cast<float*>(a.out);
           const int64_t col_n = static_cast<int64_t>(nb) * kTileN + r;
@@ -429,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float recv = __shfl_xor_sync(kFull, is_gate ? a1 : a0, 16);
             const float g = (is_gate ? a0 : recv) * alpha;
             const float up = (is_gate ? recv : a1) * alpha;
-            const float h = g / (1.0f + expf(-g)) * up;
+            // silu(g) = g / (1 + e^-g); fast exp and division keep the
+            // relative error within a few 1e-6.
+            const float h = __fdividef(g, 1.0f + __expf(-g)) * up;
             const int col = 16 * j + 2 * m + (is_gate ? 0 : 1);
             if (col < U.ntok) {
               const int64_t idx = static_cast<int64_t>(U.row0 + col) * a.ldo + i;
@@ -439,6 +430,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 static_cast<float*>(a.out)[idx] = h;
             }
           }
+        }
+      };
+      if (MT > 1) {
+        // All chunks of this warp's tile: two chunks (32 columns) per TMEM
+        // load and wait.
+        for (int j = 0; live && j < nchunks; j += 2) {
+          uint32_t v[32];
+          tmem_ld32(t_base + 16 * j, v);
+          tmem_ld_wait();
+          uint32_t v0[16], v1[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) { v0[x] = v[x]; v1[x] = v[16 + x]; }
+          emit16(v0, j);
+          if (j + 1 < nchunks) emit16(v1, j + 1);
+        }
+      } else {
+        for (int j = part; live && j < nchunks; j += 2) {
+          uint32_t v[16];
+          tmem_ld16(t_base + 16 * j, v);
+          if (C::kMmaWarps > 1) {
+            uint32_t w[16];
+            tmem_ld16(t_base + static_cast<uint32_t>(NT) + 16 * j, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
+          }
+          tmem_ld_wait();
+          emit16(v, j);
         }
       }
       tc_fence_before();
