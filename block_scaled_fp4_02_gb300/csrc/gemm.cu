@@ -62,7 +62,10 @@ struct Cfg {
   static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
   static constexpr int kAccBufs = kATmem ? 2 : 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
-  static constexpr int kDqPerStage = kATmem ? kDqWarps : kDqGroups * kDqWarps;
+  // Dequant warps per stage: NT=64 splits the 16 warps into four groups of
+  // four (one row quarter and the whole 64-wide K step each), NT=256 into
+  // two groups of eight (row quarter x K half) that fill one tile each.
+  static constexpr int kDqPerStage = kATmem ? 4 : kDqGroups * kDqWarps;
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = kAOff + kAStage * kSAa;
   static constexpr uint32_t kFOff = kBOff + kBStage * kSB;
@@ -76,6 +79,8 @@ struct Cfg {
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
                           kATmemCol + 32 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
+  static_assert(!kATmem || (kSAa == kSB && kSF % 4 == 0 && kSAa % 4 == 0),
+                "NT=64 rings: shared A/B release, four dequant groups");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
 };
@@ -109,16 +114,19 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
 }
 
 // 8 packed E2M1 codes -> 8 bf16 (4 words, element 0 in the low half of
-// word 0), each multiplied by the bf16 pair s2.  The packer places element
-// j's magnitude bits (m, e0, e1) and sign so that one or two rotates and a
-// mask put them at bf16 bits 6..8 and 15 (or 22..24 and 31): read as bf16,
-// (s, e1, e0, m) there is e2m1 * 2^-126 (code 1 = 0.5 lands on a subnormal),
-// and the multiply by s * 2^119 gives e2m1 * s * 2^-7 exactly.
+// word 0), each multiplied by the bf16 pair s2.  The packer places each
+// element's magnitude bits (m, e0, e1) and sign so that shifts and masks put
+// them at bf16 bits 6..8 and 15 (or 22..24 and 31): read as bf16, (s, e1, e0,
+// m) there is e2m1 * 2^-126 (code 1 = 0.5 lands on a subnormal), and the
+// multiply by s * 2^119 gives e2m1 * s * 2^-7 exactly.  Plain shifts (no
+// rotates) let the compiler put the left shifts on the multiply-add pipe,
+// which is less loaded than the logic pipe.
 __device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t s2) {
   const uint32_t w0 = x & 0x81C081C0u;
-  const uint32_t w1 = (rotl32(x, 3) & 0x01C001C0u) | (rotl32(x, 1) & 0x80008000u);
-  const uint32_t w2 = rotl32(x, 6) & 0x81C081C0u;
-  const uint32_t w3 = (rotl32(x, 11) & 0x01C001C0u) | (rotl32(x, 5) & 0x80008000u);
+  const uint32_t w1 = (x << 3) & 0x81C081C0u;
+  const uint32_t w2 = (x << 6) & 0x81C081C0u;
+  const uint32_t w3 = ((x >> 8) & 0x00400040u) | ((x >> 3) & 0x01800180u) |
+                      ((x << 2) & 0x80008000u);
   return make_uint4(bf16x2_mul(w0, s2), bf16x2_mul(w1, s2), bf16x2_mul(w2, s2),
                     bf16x2_mul(w3, s2));
 }
@@ -229,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
         const int nbox = (U.ntok + 15) >> 4;
         for (int ks = 0; ks < a.ksteps; ++ks) {
-          if (!mbar_wait(emptyB(s), ph ^ 1u)) { ok = false; break; }
+          // With A in TMEM the A and B rings have the same depth and one
+          // commit (on emptyA) frees both stages of a step.
+          if (!mbar_wait(C::kATmem ? emptyA(s) : emptyB(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(fullB(s), nbox * 2048u);
           const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
           for (int b = 0; b < nbox; ++b)
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           umma_commit(emptyA(sa));
-          umma_commit(emptyB(sb));
+          if (!C::kATmem) umma_commit(emptyB(sb));
         }
         if (!ok) break;
         umma_commit(accFull(buf));
@@ -302,15 +312,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) record_error(a.err, FP4MOE_ERR_TIMEOUT);
     }
+  } else if (warp < kWarpEpi0 && C::kATmem) {
+    // ------------------------------------------- dequant, A in TMEM (NT=64)
+    // Group g (four warps) takes the K steps n = g (mod 4); warp q of the
+    // group dequantizes rows 32q.. over the whole 64-wide step into TMEM
+    // lanes 32q.. (the lane quarter its warp may write).
+    const int grp = (warp - kWarpDq0) >> 2;
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol;
+    int sf = grp, sa = grp;           // ring stages of this group's next step
+    uint32_t phf = 0, pha = 0;
+    uint32_t n = 0;                   // K steps of this CTA before the unit
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      for (int ks = (grp - static_cast<int>(n)) & 3; ks < a.ksteps; ks += 4) {
+        if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
+        const uint8_t* f = smem + C::kFOff + sf * C::kFStage;
+        const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
+        const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
+        uint32_t s0, s1, s2, s3;      // bf16 scale pairs of the 16-wide groups
+        if (a.gran == 16) {
+          const uint8_t* sc = f + kTileDataBytes + r * 4;
+          s0 = sc[0] * smul2 + sadd2;
+          s1 = sc[1] * smul2 + sadd2;
+          s2 = sc[2] * smul2 + sadd2;
+          s3 = sc[3] * smul2 + sadd2;
+        } else {
+          const uint8_t* sc = f + kTileDataBytes + r * 2;
+          s0 = s1 = sc[0] * smul2 + sadd2;
+          s2 = s3 = sc[1] * smul2 + sadd2;
+        }
+        const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
+        const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
+        const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
+        const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyF(sf));
+        if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
+        tc_fence_after();             // after the MMA that last read this stage
+        const uint32_t v[32] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w,
+                                w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
+                                w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
+        tmem_st32(t_row + sa * 32u, v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aready(sa));
+        sf += 4;
+        if (sf >= SF) { sf -= SF; phf ^= 1u; }
+        sa += 4;
+        if (sa >= SAa) { sa -= SAa; pha ^= 1u; }
+      }
+      n += static_cast<uint32_t>(a.ksteps);
+    }
+    if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   } else if (warp < kWarpEpi0) {
-    // ---------------------------------------------------------- dequant
+    // ------------------------------------ dequant, A in shared memory (NT=256)
     const int dq = warp - kWarpDq0;   // 0 .. 15
     const int grp = dq / kDqWarps;
     const int w8 = dq % kDqWarps;
     const int q = warp & 3;           // row quarter = TMEM lane quarter
     const int khalf = w8 >> 2;        // 32-wide K half of each step
     const int r = 32 * q + lane;      // weight row in the tile
-    const uint32_t smul = a.smul, sadd = a.sadd;
+    const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
     const uint32_t a_row_off = (r >> 3) * 1024u + (r & 7) * 128u;
     const uint32_t sw = r & 7, cb = 4 * khalf;
     // MT = 2: group g fills weight tile g of every step; MT = 1: the groups
@@ -339,9 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             c0 = c1 = f[kTileDataBytes + r * 2 + khalf];
           }
-          uint32_t s0 = c0 * smul + sadd, s1 = c1 * smul + sadd;
-          s0 |= s0 << 16;
-          s1 |= s1 << 16;
+          // (c * smul + sadd) * 0x10001: the bf16 scale in both halves.
+          const uint32_t s0 = c0 * smul2 + sadd2, s1 = c1 * smul2 + sadd2;
           w0 = dequant8(d.x, s0); w1 = dequant8(d.y, s0);
           w2 = dequant8(d.z, s1); w3 = dequant8(d.w, s1);
         } else {

@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 // Packed tile (e, nb, ks): 128 weight rows x 64 K elements, contiguous:
 //   [0, 4096)      E2M1 data: [2 halves of 32 K][128 rows][16 bytes]; each
 //                  16-byte row half is 4 words of 8 elements whose bits are
-//                  placed so that the GEMM's dequantizer needs only rotates
+//                  placed so that the GEMM's dequantizer needs only shifts
 //                  and masks (see dequant8 in gemm.cu);
 //   [4096, ...)    scale codes: [128 rows][64 / gran bytes].
 // FC1 tiles interleave gate and up rows: in row r = 32 q + l, l < 16 is gate
@@ -519,17 +519,22 @@ __global__ void __launch_bounds__(256) combine_kernel(
 // c = b - bmax + 254 with bf16 bits c * 128 (scales more than 2^126 below the
 // matrix maximum flush to zero).
 
-// Bit positions of element j (k offset 0..7) in a packed word: the 3
-// magnitude bits start at kMagPos[j], the sign bit sits at kSgnPos[j].
-__constant__ uint8_t kMagPos[8] = {6, 22, 3, 19, 0, 16, 27, 11};
-__constant__ uint8_t kSgnPos[8] = {15, 31, 14, 30, 9, 25, 10, 26};
+// Bit positions of element j (k offset 0..7) in a packed word, for its
+// magnitude bits m, e0, e1 (E2M1 bits 0..2) and its sign: elements 0..5 keep
+// their magnitude bits contiguous and the sign 9 bits above them, so one left
+// shift and one mask place two of them as bf16 (s, e1, e0, m) at bits 15, 8,
+// 7, 6 and 31, 24, 23, 22; elements 6 and 7 need three shifts.
+__constant__ uint8_t kBitPos[8][4] = {
+    {6, 7, 8, 15},   {22, 23, 24, 31}, {3, 4, 5, 12},   {19, 20, 21, 28},
+    {0, 1, 2, 9},    {16, 17, 18, 25}, {14, 10, 11, 13}, {30, 26, 27, 29}};
 
 __device__ __forceinline__ uint32_t pack8(const uint8_t* c) {
   uint32_t x = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    x |= (static_cast<uint32_t>(c[j] & 7u) << kMagPos[j]) |
-         (static_cast<uint32_t>((c[j] >> 3) & 1u) << kSgnPos[j]);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      x |= static_cast<uint32_t>((c[j] >> b) & 1u) << kBitPos[j][b];
   return x;
 }
 

@@ -71,11 +71,11 @@ def requant_weights_oracle(orc, w, E, K, I):
 # ---------------------------------------------------------------- layout
 # Test-side decoder of the packed tile layout (independent of the packer):
 # tile (e, nb, ks) = 128 rows x 64 K; bytes [0,4096) data as
-# [half][row][16 B], each 16 B = 4 words of 8 elements; element j of a word
-# has its 3 magnitude bits starting at MAG_POS[j] and its sign at SGN_POS[j];
-# bytes [4096, ...) scale codes [row][64/gran].
-MAG_POS = [6, 22, 3, 19, 0, 16, 27, 11]
-SGN_POS = [15, 31, 14, 30, 9, 25, 10, 26]
+# [half][row][16 B], each 16 B = 4 words of 8 elements; bit b of element j's
+# E2M1 code (b = 0, 1, 2: magnitude m, e0, e1; b = 3: sign) sits at word bit
+# BIT_POS[j][b]; bytes [4096, ...) scale codes [row][64/gran].
+BIT_POS = [[6, 7, 8, 15], [22, 23, 24, 31], [3, 4, 5, 12], [19, 20, 21, 28],
+           [0, 1, 2, 9], [16, 17, 18, 25], [14, 10, 11, 13], [30, 26, 27, 29]]
 E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0.0, -.5, -1, -1.5, -2, -3, -4,
                  -6])
 
@@ -90,9 +90,10 @@ def decode_packed(buf: np.ndarray, E, N, Kd, gran, smul, sadd, alpha,
     words = data.view(np.uint32).reshape(E, nb, ks, 2, 128, 4)
     codes = np.zeros((E, nb, ks, 2, 128, 4, 8), dtype=np.uint8)
     for j in range(8):
-        mag = (words >> np.uint32(MAG_POS[j])) & np.uint32(7)
-        sgn = (words >> np.uint32(SGN_POS[j])) & np.uint32(1)
-        codes[..., j] = (mag | (sgn << 3)).astype(np.uint8)
+        c = np.zeros(words.shape, dtype=np.uint32)
+        for b in range(4):
+            c |= ((words >> np.uint32(BIT_POS[j][b])) & np.uint32(1)) << np.uint32(b)
+        codes[..., j] = c.astype(np.uint8)
     # -> [E, nb, 128 rows, ks, 64 k]
     codes = codes.transpose(0, 1, 4, 2, 3, 5, 6).reshape(E, nb, 128, ks, 64)
     sc = t[..., 4096:].reshape(E, nb, ks, 128, 64 // gran).astype(np.uint32)
