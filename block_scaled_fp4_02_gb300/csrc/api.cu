@@ -66,14 +66,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols] read in boxes of 16 rows x 64 columns with the
-// 128-byte swizzle (the UMMA K-major operand layout).
-bool make_row_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// Row-major bf16 [rows, cols] read in boxes of box_rows rows x 64 columns
+// with the 128-byte swizzle (the UMMA K-major operand layout).
+bool make_row_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn || rows == 0) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -428,7 +429,9 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 
   CUtensorMap tm_x, tm_h;
-  if (!make_row_tmap(&tm_x, xperm, P, p->K) || !make_row_tmap(&tm_h, h, P, p->I))
+  const uint32_t box_rows = static_cast<uint32_t>(gemm_box_rows(chunk));
+  if (!make_row_tmap(&tm_x, xperm, P, p->K, box_rows) ||
+      !make_row_tmap(&tm_h, h, P, p->I, box_rows))
     return FP4MOE_ERR_CUDA;
   GemmArgs a1{};
   a1.wpack = p->w13; a1.alpha = p->alpha; a1.offsets = offsets; a1.cstart = cstart;

@@ -59,6 +59,9 @@ struct Cfg {
   static constexpr uint32_t kFStage = kFBytes * kMT;
   static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
   static constexpr uint32_t kBStage = NT * 128;    // NT rows x 64 bf16
+  // Activation rows per TMA box (the tensor map is built to match): boxes
+  // of 64 rows cut the copies per step four-fold for many-token chunks.
+  static constexpr int kBoxRows = kATmem ? 16 : 64;
   static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
   static constexpr int kAccBufs = kATmem ? 2 : 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
@@ -235,15 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
-        const int nbox = (U.ntok + 15) >> 4;
+        const int nbox = (U.ntok + C::kBoxRows - 1) / C::kBoxRows;
+        constexpr uint32_t kBoxBytes = C::kBoxRows * 128u;
         for (int ks = 0; ks < a.ksteps; ++ks) {
           // With A in TMEM the A and B rings have the same depth and one
           // commit (on emptyA) frees both stages of a step.
           if (!mbar_wait(C::kATmem ? emptyA(s) : emptyB(s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(fullB(s), nbox * 2048u);
+          mbar_arrive_expect_tx(fullB(s), nbox * kBoxBytes);
           const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
+          // Rows past the chunk (up to the box) are loaded but not used;
+          // rows past the tensor are zero-filled by the TMA unit.
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(dst + b * 2048u, &tmB, ks * kTileK, U.row0 + 16 * b, fullB(s));
+            tma_load_2d(dst + b * kBoxBytes, &tmB, ks * kTileK, U.row0 + C::kBoxRows * b,
+                        fullB(s));
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
           if (++s == SB) { s = 0; ph ^= 1u; }
@@ -574,6 +581,8 @@ cudaError_t launch_nt(const CUtensorMap& tmB, const GemmArgs& a, int grid,
 }  // namespace
 
 int gemm_chunk_max(int T) { return T <= 64 ? 64 : 256; }
+
+int gemm_box_rows(int chunk) { return chunk <= 64 ? Cfg<64>::kBoxRows : Cfg<256>::kBoxRows; }
 
 cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
                         int num_sms, cudaStream_t st) {

@@ -90,6 +90,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
 
 // Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
 int gemm_chunk_max(int T);
+// Rows per TMA box of the activation tensor map for that chunk size.
+int gemm_box_rows(int chunk);
 
 // Device address of the per-device status word (kernels record errors there).
 int* status_word();
