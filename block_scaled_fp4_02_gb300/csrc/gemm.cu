@@ -10,21 +10,30 @@
 //   NT = 256 (many tokens per expert): MT = 2 weight tiles share each
 //     activation tile, which halves activation traffic per MMA; A in shared
 //     memory; two accumulators of 256 columns fill TMEM.
-//   NT = 64 (decode): MT = 1; each MMA is short and costs a fixed ~90 cycles
-//     to issue, so A lives in TMEM and two MMA warps take alternate K steps
-//     into their own accumulators (summed in the epilogue), double-buffered.
+//   NT = 32 (decode): MT = 1; A lives in TMEM.  One thread issues an
+//     asynchronous instruction (tcgen05.mma, a TMA copy) only every ~100
+//     cycles or more, far below what the tensor and TMA units take, so the
+//     issue is spread: four MMA warps take K steps n = 0..3 (mod 4) into
+//     their own accumulators (summed in the epilogue, double-buffered), two
+//     threads load the activation rows (even and odd steps), and each weight
+//     copy brings two K steps.
 // Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
-//                 (MT per 64-wide K step) into a ring of F stages;
-//   warp 1 (+27): TMEM allocation and the UMMA-issuing thread(s)
-//                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16);
+//                 (MT per K step, or two K steps with NT = 32) into a ring of
+//                 F stages;
+//   warp 1      : TMEM allocation; with NT = 256 the UMMA-issuing thread
+//                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16),
+//                 with NT = 32 the activation producer of the odd K steps;
 //   warp 2      : activation producer -- TMA of the token rows of each K step
-//                 into the B part of a ring of A/B stages;
-//   warps 3..18 : dequantizers in two groups of eight (within a group, warp w
-//                 owns rows 32*(w%4).. and one 32-wide K half of the step):
-//                 with MT = 2 group g fills weight tile g of every step, with
-//                 MT = 1 the groups take alternate steps;
-//   warps 19..26: epilogue, reading the TMEM accumulators.
+//                 (even steps with NT = 32) into the B part of a ring of A/B
+//                 stages;
+//   warps 3..18 : dequantizers: NT = 256, two groups of eight (warp w owns
+//                 rows 32*(w%4).. and one 32-wide K half; group g fills
+//                 weight tile g of every step); NT = 32, four groups of four
+//                 (whole K step; group g takes steps n = g (mod 4));
+//   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
+//                 reading the TMEM accumulators; NT = 32 then has its four
+//                 MMA warps, one per SM sub-partition.
 // All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
 // the device status word and the CTA winds down and frees its TMEM.
 #include "common.cuh"
@@ -34,14 +43,10 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kDqGroups = 2;     // dequant groups
-constexpr int kDqWarps = 8;      // warps per dequant group
-constexpr int kEpiWarps = 8;
+constexpr int kDqGroups = 2;     // dequant groups (A in shared memory)
+constexpr int kDqWarps = 8;      // warps per dequant group (A in shared memory)
 constexpr int kWarpFProd = 0, kWarpMma = 1, kWarpBProd = 2, kWarpDq0 = 3,
-              kWarpEpi0 = kWarpDq0 + kDqGroups * kDqWarps,
-              kWarpMma2 = kWarpEpi0 + kEpiWarps;
-constexpr int kWarps = kWarpMma2 + 1;
-constexpr int kThreads = kWarps * 32;
+              kWarpEpi0 = kWarpDq0 + kDqGroups * kDqWarps;
 constexpr uint32_t kABytes = kTileN * kTileK * 2;  // 16 KB bf16 tile
 constexpr uint32_t kFBytes = 4608;                 // >= largest packed tile
 constexpr uint32_t kTmemCols = 512;
@@ -50,13 +55,23 @@ template <int NT>
 struct Cfg {
   static constexpr bool kATmem = NT <= 64;         // A stages in TMEM
   static constexpr int kMT = kATmem ? 1 : 2;       // weight tiles per unit
-  static constexpr int kMmaWarps = kATmem ? 2 : 1;
+  // One thread issues a tcgen05.mma about every 55 cycles whatever its size,
+  // while the tensor pipe takes a short (N <= 32, A in TMEM) one every ~14:
+  // with A in TMEM four warps issue, one per SM sub-partition (warp % 4).
+  static constexpr int kMmaWarps = !kATmem ? 1 : (NT <= 32 ? 4 : 2);
+  static constexpr int kEpiWarps = kATmem ? 4 : 8;
+  // First MMA warp: warp 1 (shared-memory A) or the four warps after the
+  // epilogue (TMEM A; warp 1 then only allocates TMEM).
+  static constexpr int kWarpMmaX0 = kWarpEpi0 + kEpiWarps;
+  static constexpr int kWarps = kATmem ? kWarpMmaX0 + kMmaWarps : kWarpMmaX0;
+  static constexpr int kThreads = kWarps * 32;
   // Rings: F (packed weights, from HBM), A (dequantized weights, shared
   // memory or TMEM), B (activation rows, from L2 by TMA).
-  static constexpr int kSF = kATmem ? 24 : 6;
-  static constexpr int kSAa = kATmem ? 8 : 2;      // NT=64: 8 x 32 TMEM cols
+  static constexpr int kStepsPerF = kATmem ? 2 : 1;  // K steps per F stage
+  static constexpr int kSF = kATmem ? 12 : 6;
+  static constexpr int kSAa = kATmem ? 8 : 2;      // TMEM A: 8 x 32 columns
   static constexpr int kSB = kATmem ? 8 : 3;
-  static constexpr uint32_t kFStage = kFBytes * kMT;
+  static constexpr uint32_t kFStage = kFBytes * kMT * kStepsPerF;
   static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
   static constexpr uint32_t kBStage = NT * 128;    // NT rows x 64 bf16
   // Activation rows per TMA box (the tensor map is built to match): boxes
@@ -65,10 +80,12 @@ struct Cfg {
   static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
   static constexpr int kAccBufs = kATmem ? 2 : 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
-  // Dequant warps per stage: NT=64 splits the 16 warps into four groups of
+  // Dequant warps per stage: TMEM A splits the 16 warps into four groups of
   // four (one row quarter and the whole 64-wide K step each), NT=256 into
   // two groups of eight (row quarter x K half) that fill one tile each.
   static constexpr int kDqPerStage = kATmem ? 4 : kDqGroups * kDqWarps;
+  // F stages are released by both groups whose steps they hold.
+  static constexpr int kDqPerF = kATmem ? 8 : kDqGroups * kDqWarps;
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = kAOff + kAStage * kSAa;
   static constexpr uint32_t kFOff = kBOff + kBStage * kSB;
@@ -82,8 +99,8 @@ struct Cfg {
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
                           kATmemCol + 32 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
-  static_assert(!kATmem || (kSAa == kSB && kSF % 4 == 0 && kSAa % 4 == 0),
-                "NT=64 rings: shared A/B release, four dequant groups");
+  static_assert(!kATmem || (kSAa == kSB && kSF % 2 == 0 && kSAa % 4 == 0),
+                "TMEM A rings: shared A/B release, four dequant groups");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
 };
@@ -141,7 +158,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
   using C = Cfg<NT>;
   constexpr int SF = C::kSF, SAa = C::kSAa, SB = C::kSB, MT = C::kMT;
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SF; ++s) {
       mbar_init(fullF(s), 1);
-      mbar_init(emptyF(s), C::kDqPerStage);
+      mbar_init(emptyF(s), C::kDqPerF);
     }
     for (int s = 0; s < SAa; ++s) {
       mbar_init(aready(s), C::kDqPerStage);
@@ -185,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(accFull(b), C::kMmaWarps);
-      mbar_init(accEmpty(b), kEpiWarps);
+      mbar_init(accEmpty(b), C::kEpiWarps);
     }
     mbar_init(done_bar, C::kMmaWarps);
     fence_barrier_init();
@@ -213,13 +230,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
         const int64_t tstride = static_cast<int64_t>(a.ksteps) * a.tile_bytes;
-        for (int ks = 0; ks < a.ksteps; ++ks) {
+        // TMEM A: one copy of two consecutive K-step tiles per stage (one
+        // 4.6 KB copy per step cannot keep HBM busy; ksteps is even).
+        for (int ks = 0; ks < a.ksteps; ks += C::kStepsPerF) {
           if (!mbar_wait(emptyF(s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(fullF(s), tiles * a.tile_bytes);
-          for (int t = 0; t < tiles; ++t)
-            bulk_load(sbase + C::kFOff + s * C::kFStage + t * kFBytes,
-                      wt + t * tstride + static_cast<int64_t>(ks) * a.tile_bytes,
-                      a.tile_bytes, fullF(s));
+          if (C::kATmem) {
+            mbar_arrive_expect_tx(fullF(s), 2 * a.tile_bytes);
+            bulk_load(sbase + C::kFOff + s * C::kFStage,
+                      wt + static_cast<int64_t>(ks) * a.tile_bytes, 2 * a.tile_bytes,
+                      fullF(s));
+          } else {
+            mbar_arrive_expect_tx(fullF(s), tiles * a.tile_bytes);
+            for (int t = 0; t < tiles; ++t)
+              bulk_load(sbase + C::kFOff + s * C::kFStage + t * kFBytes,
+                        wt + t * tstride + static_cast<int64_t>(ks) * a.tile_bytes,
+                        a.tile_bytes, fullF(s));
+          }
           issued |= 1u << (s & 31);
           issued_ph = (issued_ph & ~(1u << (s & 31))) | (ph << (s & 31));
           if (++s == SF) { s = 0; ph ^= 1u; }
@@ -230,19 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < SF && t < 32; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullF(t), (issued_ph >> t) & 1u);
     }
-  } else if (warp == kWarpBProd) {
-    // --------------------------------------------- activation producer
+  } else if (warp == kWarpBProd || (C::kATmem && warp == kWarpMma)) {
+    // --------------------------------------------- activation producer(s)
     if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0, issued = 0, issued_ph = 0;
+      const int nprod = C::kATmem ? 2 : 1;
+      const int bp = (warp == kWarpBProd) ? 0 : 1;
+      uint32_t n = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
         const int nbox = (U.ntok + C::kBoxRows - 1) / C::kBoxRows;
         constexpr uint32_t kBoxBytes = C::kBoxRows * 128u;
-        for (int ks = 0; ks < a.ksteps; ++ks) {
-          // With A in TMEM the A and B rings have the same depth and one
-          // commit (on emptyA) frees both stages of a step.
+        for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
+          if (static_cast<int>(n % nprod) != bp) continue;
+          const int s = static_cast<int>(n % SB);
+          const uint32_t ph = (n / SB) & 1u;
           if (!mbar_wait(C::kATmem ? emptyA(s) : emptyB(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(fullB(s), nbox * kBoxBytes);
           const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
@@ -253,17 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fullB(s));
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
-          if (++s == SB) { s = 0; ph ^= 1u; }
         }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
       for (int t = 0; t < SB; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
     }
-  } else if (warp == kWarpMma || warp == kWarpMma2) {
+  } else if (C::kATmem ? warp >= C::kWarpMmaX0 : warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
-    const int mi = (warp == kWarpMma) ? 0 : 1;   // takes K steps n % kMmaWarps == mi
-    if (mi < C::kMmaWarps && lane == 0) {
+    const int mi = C::kATmem ? warp - C::kWarpMmaX0 : 0;  // takes K steps n % kMmaWarps == mi
+    if (lane == 0) {
       int buf = 0;
       uint32_t n = 0, acc_ph = 0;
       bool ok = true;
@@ -319,8 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) record_error(a.err, FP4MOE_ERR_TIMEOUT);
     }
+  } else if (warp == kWarpMma) {
+    // Not reached: with TMEM A warp 1 is an activation producer.
   } else if (warp < kWarpEpi0 && C::kATmem) {
-    // ------------------------------------------- dequant, A in TMEM (NT=64)
+    // ------------------------------------------- dequant, A in TMEM (NT=32)
     // Group g (four warps) takes the K steps n = g (mod 4); warp q of the
     // group dequantizes rows 32q.. over the whole 64-wide step into TMEM
     // lanes 32q.. (the lane quarter its warp may write).
@@ -329,14 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * q + lane;
     const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol;
-    int sf = grp, sa = grp;           // ring stages of this group's next step
+    // Step n sits in F stage n / 2 at tile offset (n % 2) * tile_bytes.
+    int sf = grp >> 1, sa = grp;      // ring stages of this group's next step
+    const uint32_t f_off = static_cast<uint32_t>(grp & 1) * static_cast<uint32_t>(a.tile_bytes);
     uint32_t phf = 0, pha = 0;
     uint32_t n = 0;                   // K steps of this CTA before the unit
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       for (int ks = (grp - static_cast<int>(n)) & 3; ks < a.ksteps; ks += 4) {
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        const uint8_t* f = smem + C::kFOff + sf * C::kFStage;
+        const uint8_t* f = smem + C::kFOff + sf * C::kFStage + f_off;
         const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
         const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
         uint32_t s0, s1, s2, s3;      // bf16 scale pairs of the 16-wide groups
@@ -351,24 +382,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           s0 = s1 = sc[0] * smul2 + sadd2;
           s2 = s3 = sc[1] * smul2 + sadd2;
         }
-        const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
-        const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
-        const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
-        const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(emptyF(sf));
+        // The A stage must be free before the first TMEM store; the F stage
+        // is released once both K halves have been converted.
         if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
         tc_fence_after();             // after the MMA that last read this stage
-        const uint32_t v[32] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w,
-                                w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
-                                w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
-        tmem_st32(t_row + sa * 32u, v);
+        const uint32_t t_st = t_row + sa * 32u;
+        {
+          const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
+          const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
+          const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                  w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+          tmem_st16(t_st, v);
+        }
+        {
+          const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
+          const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
+          const uint32_t v[16] = {w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
+                                  w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
+          tmem_st16(t_st + 16u, v);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyF(sf));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(aready(sa));
-        sf += 4;
+        sf += 2;
         if (sf >= SF) { sf -= SF; phf ^= 1u; }
         sa += 4;
         if (sa >= SAa) { sa -= SAa; pha ^= 1u; }
@@ -450,14 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   } else {
     // --------------------------------------------------------- epilogue
-    const int ew = warp - kWarpEpi0;  // 0..7
+    const int ew = warp - kWarpEpi0;  // 0 .. kEpiWarps-1
     const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int part = ew >> 2;         // MT = 2: weight tile; MT = 1: column half
+    constexpr int kParts = C::kEpiWarps / 4;
+    const int part = ew >> 2;         // MT = 2: weight tile; MT = 1: column slice
     const int r = 32 * q + lane;      // weight row in the tile
     int buf = 0;
     uint32_t acc_ph = 0;
+    uint32_t n_unit = 0;              // K steps of this CTA before the unit
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, n_unit += a.ksteps) {
       const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
       if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
@@ -519,18 +560,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < nchunks) emit16(v1, j + 1);
         }
       } else {
-        for (int j = part; live && j < nchunks; j += 2) {
+        // Sum the partial accumulators (NT columns apart) of the MMA warps
+        // that had K steps in this unit: warp m took the steps with
+        // (n_unit + ks) % kMmaWarps == m, none when ksteps is short.
+        const int m0 = static_cast<int>(n_unit % C::kMmaWarps);
+        const int nparts = min(C::kMmaWarps, a.ksteps);
+        for (int j = part; live && j < nchunks; j += kParts) {
           uint32_t v[16];
-          tmem_ld16(t_base + 16 * j, v);
-          if (C::kMmaWarps > 1) {
+          tmem_ld16(t_base + static_cast<uint32_t>(m0 * NT) + 16 * j, v);
+          tmem_ld_wait();
+          for (int p = 1; p < nparts; ++p) {
+            const int m = (m0 + p) % C::kMmaWarps;
             uint32_t w[16];
-            tmem_ld16(t_base + static_cast<uint32_t>(NT) + 16 * j, w);
+            tmem_ld16(t_base + static_cast<uint32_t>(m * NT) + 16 * j, w);
             tmem_ld_wait();
 #pragma unroll
             for (int x = 0; x < 16; ++x)
               v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
           }
-          tmem_ld_wait();
           emit16(v, j);
         }
       }
@@ -564,7 +611,7 @@ cudaError_t launch_one(const CUtensorMap& tmB, const GemmArgs& a, int grid,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  moe_gemm_kernel<NT, MODE><<<grid, kThreads, Cfg<NT>::kSmem, st>>>(tmB, a);
+  moe_gemm_kernel<NT, MODE><<<grid, Cfg<NT>::kThreads, Cfg<NT>::kSmem, st>>>(tmB, a);
   return cudaGetLastError();
 }
 
@@ -580,14 +627,14 @@ cudaError_t launch_nt(const CUtensorMap& tmB, const GemmArgs& a, int grid,
 
 }  // namespace
 
-int gemm_chunk_max(int T) { return T <= 64 ? 64 : 256; }
+int gemm_chunk_max(int T) { return T <= 64 ? 32 : 256; }
 
-int gemm_box_rows(int chunk) { return chunk <= 64 ? Cfg<64>::kBoxRows : Cfg<256>::kBoxRows; }
+int gemm_box_rows(int chunk) { return chunk <= 32 ? Cfg<32>::kBoxRows : Cfg<256>::kBoxRows; }
 
 cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
                         int num_sms, cudaStream_t st) {
   const int grid = num_sms > 0 ? num_sms : 1;
-  if (nt <= 64) return launch_nt<64>(tmB, a, grid, st);
+  if (nt <= 32) return launch_nt<32>(tmB, a, grid, st);
   return launch_nt<256>(tmB, a, grid, st);
 }
 
