@@ -14,26 +14,27 @@
 //     asynchronous instruction (tcgen05.mma, a TMA copy) only every ~100
 //     cycles or more, far below what the tensor and TMA units take, so the
 //     issue is spread: four MMA warps take K steps n = 0..3 (mod 4) into
-//     their own accumulators (summed in the epilogue, double-buffered), two
-//     threads load the activation rows (even and odd steps), and each weight
-//     copy brings two K steps.
+//     their own accumulators (summed in the epilogue, double-buffered), four
+//     threads load the activation rows (steps n = 0..3 (mod 4)), and each
+//     weight copy brings two K steps.
 // Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
 //                 (MT per K step, or two K steps with NT = 32) into a ring of
 //                 F stages;
 //   warp 1      : TMEM allocation; with NT = 256 the UMMA-issuing thread
 //                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16),
-//                 with NT = 32 the activation producer of the odd K steps;
+//                 with NT = 32 the activation producer of steps n = 1 (mod 4);
 //   warp 2      : activation producer -- TMA of the token rows of each K step
-//                 (even steps with NT = 32) into the B part of a ring of A/B
-//                 stages;
+//                 (steps n = 0 (mod 4) with NT = 32) into the B part of a ring
+//                 of A/B stages;
 //   warps 3..18 : dequantizers: NT = 256, two groups of eight (warp w owns
 //                 rows 32*(w%4).. and one 32-wide K half; group g fills
 //                 weight tile g of every step); NT = 32, four groups of four
 //                 (whole K step; group g takes steps n = g (mod 4));
 //   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
 //                 reading the TMEM accumulators; NT = 32 then has its four
-//                 MMA warps, one per SM sub-partition.
+//                 MMA warps, one per SM sub-partition, and the activation
+//                 producers of steps n = 2, 3 (mod 4).
 // All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
 // the device status word and the CTA winds down and frees its TMEM.
 #include "common.cuh"
@@ -63,7 +64,9 @@ struct Cfg {
   // First MMA warp: warp 1 (shared-memory A) or the four warps after the
   // epilogue (TMEM A; warp 1 then only allocates TMEM).
   static constexpr int kWarpMmaX0 = kWarpEpi0 + kEpiWarps;
-  static constexpr int kWarps = kATmem ? kWarpMmaX0 + kMmaWarps : kWarpMmaX0;
+  static constexpr int kWarpBX0 = kWarpMmaX0 + kMmaWarps;   // extra B producers
+  static constexpr int kExtraB = kATmem ? 2 : 0;
+  static constexpr int kWarps = kATmem ? kWarpBX0 + kExtraB : kWarpMmaX0;
   static constexpr int kThreads = kWarps * 32;
   // Rings: F (packed weights, from HBM), A (dequantized weights, shared
   // memory or TMEM), B (activation rows, from L2 by TMA).
@@ -256,11 +259,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       for (int t = 0; t < SF && t < 32; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullF(t), (issued_ph >> t) & 1u);
     }
-  } else if (warp == kWarpBProd || (C::kATmem && warp == kWarpMma)) {
+  } else if (warp == kWarpBProd || (C::kATmem && (warp == kWarpMma || warp >= C::kWarpBX0))) {
     // --------------------------------------------- activation producer(s)
     if (lane == 0) {
-      const int nprod = C::kATmem ? 2 : 1;
-      const int bp = (warp == kWarpBProd) ? 0 : 1;
+      const int nprod = C::kATmem ? 2 + C::kExtraB : 1;
+      const int bp = (warp == kWarpBProd) ? 0 : (warp == kWarpMma) ? 1 : 2 + (warp - C::kWarpBX0);
       uint32_t n = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
