@@ -9,7 +9,8 @@
 // in the 128-byte swizzled layout.  Two variants:
 //   NT = 256 (many tokens per expert): MT = 2 weight tiles share each
 //     activation tile, which halves activation traffic per MMA; A in shared
-//     memory; two accumulators of 256 columns fill TMEM.
+//     memory; two accumulators of 256 columns fill TMEM; one MMA warp per
+//     tile.
 //   NT = 32 (decode): MT = 1; A lives in TMEM.  One thread issues an
 //     asynchronous instruction (tcgen05.mma, a TMA copy) only every ~100
 //     cycles or more, far below what the tensor and TMA units take, so the
@@ -21,9 +22,10 @@
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
 //                 (MT per K step, or two K steps with NT = 32) into a ring of
 //                 F stages;
-//   warp 1      : TMEM allocation; with NT = 256 the UMMA-issuing thread
-//                 (kind::f16, M = 128, N = tokens rounded up to 16, K = 16),
-//                 with NT = 32 the activation producer of steps n = 1 (mod 4);
+//   warp 1      : TMEM allocation; with NT = 256 the UMMA-issuing thread of
+//                 tile 0 (kind::f16, M = 128, N = tokens rounded up to 16,
+//                 K = 16), with NT = 32 the activation producer of steps
+//                 n = 1 (mod 4);
 //   warp 2      : activation producer -- TMA of the token rows of each K step
 //                 (steps n = 0 (mod 4) with NT = 32) into the B part of a ring
 //                 of A/B stages;
@@ -32,9 +34,10 @@
 //                 weight tile g of every step); NT = 32, four groups of four
 //                 (whole K step; group g takes steps n = g (mod 4));
 //   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
-//                 reading the TMEM accumulators; NT = 32 then has its four
-//                 MMA warps, one per SM sub-partition, and the activation
-//                 producers of steps n = 2, 3 (mod 4).
+//                 reading the TMEM accumulators; then NT = 256 has the MMA
+//                 warp of tile 1, NT = 32 its four MMA warps (one per SM
+//                 sub-partition) and the activation producers of steps
+//                 n = 2, 3 (mod 4).
 // All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
 // the device status word and the CTA winds down and frees its TMEM.
 #include "common.cuh"
@@ -59,14 +62,16 @@ struct Cfg {
   // One thread issues a tcgen05.mma about every 55 cycles whatever its size,
   // while the tensor pipe takes a short (N <= 32, A in TMEM) one every ~14:
   // with A in TMEM four warps issue, one per SM sub-partition (warp % 4).
-  static constexpr int kMmaWarps = !kATmem ? 1 : (NT <= 32 ? 4 : 2);
+  // With A in shared memory two MMA warps each own one weight tile (all K
+  // steps); with A in TMEM the MMA warps split the K steps.
+  static constexpr int kMmaWarps = !kATmem ? 2 : (NT <= 32 ? 4 : 2);
   static constexpr int kEpiWarps = kATmem ? 4 : 8;
   // First MMA warp: warp 1 (shared-memory A) or the four warps after the
   // epilogue (TMEM A; warp 1 then only allocates TMEM).
   static constexpr int kWarpMmaX0 = kWarpEpi0 + kEpiWarps;
   static constexpr int kWarpBX0 = kWarpMmaX0 + kMmaWarps;   // extra B producers
   static constexpr int kExtraB = kATmem ? 2 : 0;
-  static constexpr int kWarps = kATmem ? kWarpBX0 + kExtraB : kWarpMmaX0;
+  static constexpr int kWarps = kATmem ? kWarpBX0 + kExtraB : kWarpMmaX0 + 1;
   static constexpr int kThreads = kWarps * 32;
   // Rings: F (packed weights, from HBM), A (dequantized weights, shared
   // memory or TMEM), B (activation rows, from L2 by TMA).
@@ -197,11 +202,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     }
     for (int s = 0; s < SAa; ++s) {
       mbar_init(aready(s), C::kDqPerStage);
-      mbar_init(emptyA(s), 1);
+      mbar_init(emptyA(s), C::kATmem ? 1 : C::kMmaWarps);
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(fullB(s), 1);
-      mbar_init(emptyB(s), 1);
+      mbar_init(emptyB(s), C::kATmem ? 1 : C::kMmaWarps);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(accFull(b), C::kMmaWarps);
@@ -290,9 +295,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       for (int t = 0; t < SB; ++t)
         if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
     }
-  } else if (C::kATmem ? warp >= C::kWarpMmaX0 : warp == kWarpMma) {
+  } else if (C::kATmem ? warp >= C::kWarpMmaX0
+                        : (warp == kWarpMma || warp == C::kWarpMmaX0)) {
     // ---------------------------------------------------------------- MMA
-    const int mi = C::kATmem ? warp - C::kWarpMmaX0 : 0;  // takes K steps n % kMmaWarps == mi
+    // TMEM A: warp mi takes K steps n % kMmaWarps == mi; shared-memory A:
+    // warp mi issues the MMAs of weight tile mi in every step.
+    const int mi = C::kATmem ? warp - C::kWarpMmaX0 : (warp == kWarpMma ? 0 : 1);
     if (lane == 0) {
       int buf = 0;
       uint32_t n = 0, acc_ph = 0;
@@ -310,7 +318,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         tc_fence_after();
         uint32_t acc = 0;
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
-          if (static_cast<int>(n % C::kMmaWarps) != mi) continue;
+          if (C::kATmem && static_cast<int>(n % C::kMmaWarps) != mi) continue;
           const int sa = static_cast<int>(n % SAa), sb = static_cast<int>(n % SB);
           if (!mbar_wait(fullB(sb), (n / SB) & 1u) || !mbar_wait(aready(sa), (n / SAa) & 1u)) {
             ok = false;
@@ -327,13 +335,13 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
               umma_f16_ta(d_tmem, at + kk * 8u, bd + 2u * kk, idesc, acc);
               acc = 1u;
             }
-          } else {
-            const uint64_t ad = adesc0 + static_cast<uint64_t>((sa * C::kAStage) >> 4);
+          } else if (mi < tiles) {
+            // Tile mi -> accumulator columns 256 mi (d_tmem).
+            const uint64_t ad = adesc0 + static_cast<uint64_t>((sa * C::kAStage) >> 4) +
+                                (kABytes >> 4) * static_cast<uint32_t>(mi);
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
-              for (int t = 0; t < tiles; ++t)   // tile t -> accumulator columns 256 t
-                umma_f16(d_tmem + 256u * t, ad + (kABytes >> 4) * t + 2u * kk,
-                         bd + 2u * kk, idesc, acc);
+              umma_f16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
               acc = 1u;
             }
           }
