@@ -20,6 +20,7 @@ sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -274,6 +275,28 @@ class MoeRun:
         self.packed.free()
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_moe_gemm_fc1.json")
+
+
+def measured_traffic(workload: str):
+    """FC1 DRAM bytes per launch from the committed ncu capture (scaled
+    from a small case, see the file), or None when the GEMM sources have
+    changed since the capture or no capture covers this workload."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        h = hashlib.sha256()
+        for rel in t["source_files"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != t["source_sha256"]:
+            return None
+        entry = t["per_launch_bytes"].get(workload)
+        return None if entry is None else float(entry["bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src, long_step):
     cfg = run.cfg
     s = total_ms / 1e3
@@ -294,7 +317,8 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src, long_step):
                 "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_source": f"{pk_src} {peak_key}",
                 "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
-                "per_launch_flops": fc1_flops}
+                "per_launch_flops": fc1_flops,
+                "per_launch_bytes": run.fc1_bytes()}
     else:
         ach = run.fc1_bytes() / (fc1_ms / 1e3) / 1e9
         peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -302,6 +326,7 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src, long_step):
                 "frac": ach / peak, "peak_source": f"{pk_src} hbm_gbs",
                 "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
                 "per_launch_bytes": run.fc1_bytes()}
+    roof["traffic"] = measured_traffic(cfg.name)
     out["layer_hbm_frac"] = wgbs / float(pk.get("hbm_gbs", 6800.0))
     return out, roof
 
@@ -440,8 +465,6 @@ def main():
         total_ms = float(t.item())
     head, roof = summarize(run, total_ms, stages, args.steps, pk, pk_src,
                            long_step=True)
-    traffic = None
-    roof["traffic"] = traffic
 
     e2e = None
     if not args.no_e2e:
