@@ -28,71 +28,48 @@ int num_sms() {
 // group16 -> group32 requant ("glm52_nvfp4_group16_notes.md", section
 // "Requantization path").  One thread owns one 32-element group: 16 bytes of
 // codes and two E4M3 scales in, 16 bytes of codes and one UE8M0 byte out.
-// Because the scale of a half is constant, the new code of each element
-// depends only on its half, its 3-bit magnitude and its sign.  The thread
-// builds, per half, an 8-entry table new_mag[m] = RNE(e2m1(m) * |s| / 2^e)
-// with the hardware E2M1 conversion, maps all 32 nibbles through it with byte
-// permutes, and passes the sign through (flipped for a negative scale).
+// The codes are widened to exact f16 pairs with the hardware E2M1
+// conversion, the group maximum |e2m1| * |s| picks the UE8M0 exponent e, each
+// half is multiplied by s / 2^e in f16 (exact: at most six significant bits)
+// and converted back with round-to-nearest-even, which keeps the sign (also
+// of zero) and flips it for a negative scale.
 
-// E2M1 magnitude of a 3-bit code, exactly: placing (e1 e0 m) at float bits
-// 24..22 gives e2m1 * 2^-126, including the subnormal code 1 (0.5).
-__device__ __forceinline__ float e2m1_mag(uint32_t m) {
-  return __uint_as_float(m << 22) * 0x1p126f;
+// Four packed E2M1 pairs (the bytes of w) -> four f16x2 (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
-// Largest 3-bit magnitude among the 16 nibbles of two words, from bit tests
-// that hold for any nibble: bit 2 of (x & x<<1) is "m >= 6", of
-// (x & x<<1 & x<<2) "m == 7", of (x & (x<<1 | x<<2)) "m >= 5"; for nibbles
-// below 4, bit 1 of (x & x<<1) is "m == 3".
-__device__ __forceinline__ uint32_t max_mag16(uint32_t x, uint32_t y) {
-  const uint32_t b2 = 0x44444444u, b1 = 0x22222222u;
-  const uint32_t hx = x & (x << 1), hy = y & (y << 1);
-  const uint32_t any = x | y;
-  uint32_t m;
-  if (any & b2) {
-    const bool c7 = ((hx & (x << 2)) | (hy & (y << 2))) & b2;
-    const bool c6 = (hx | hy) & b2;
-    const bool c5 = ((x & ((x << 1) | (x << 2))) | (y & ((y << 1) | (y << 2)))) & b2;
-    m = c7 ? 7u : c6 ? 6u : c5 ? 5u : 4u;
-  } else {
-    const bool c3 = (hx | hy) & b1;
-    m = c3 ? 3u : (any & b1) ? 2u : (any & 0x11111111u) ? 1u : 0u;
-  }
-  return m;
+// Four f16x2 -> four packed E2M1 pairs (RNE, saturating; sign of zero kept).
+__device__ __forceinline__ uint32_t f16x8_to_e2m1x8(const uint32_t (&h)[4]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f16x2 b0, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f16x2 b1, %2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f16x2 b2, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f16x2 b3, %4;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]));
+  return w;
 }
 
-// Two non-negative f32 -> two E2M1 codes (RNE, saturating), lo in the low
-// nibble.
-__device__ __forceinline__ uint32_t pos_f32x2_to_e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "cvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
+__device__ __forceinline__ uint32_t hmax_abs2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// Table of new magnitudes for f = |s| / 2^e: byte m of (lo, hi) = new mag m.
-__device__ __forceinline__ void build_lut(float f, uint32_t& lo, uint32_t& hi) {
-  const uint32_t c01 = pos_f32x2_to_e2m1x2(0.0f, 0.5f * f);
-  const uint32_t c23 = pos_f32x2_to_e2m1x2(1.0f * f, 1.5f * f);
-  const uint32_t c45 = pos_f32x2_to_e2m1x2(2.0f * f, 3.0f * f);
-  const uint32_t c67 = pos_f32x2_to_e2m1x2(4.0f * f, 6.0f * f);
-  lo = (c01 & 0x7u) | ((c01 & 0x70u) << 4) | ((c23 & 0x7u) << 16) |
-       ((c23 & 0x70u) << 20);
-  hi = (c45 & 0x7u) | ((c45 & 0x70u) << 4) | ((c67 & 0x7u) << 16) |
-       ((c67 & 0x70u) << 20);
-}
-
-// Maps the 8 nibbles of w through the table; sign bits pass through XOR sx.
-__device__ __forceinline__ uint32_t remap8(uint32_t w, uint32_t lo, uint32_t hi,
-                                           uint32_t sx) {
-  const uint32_t r0 = __byte_perm(lo, hi, w & 0x7777u);
-  const uint32_t r1 = __byte_perm(lo, hi, (w >> 16) & 0x7777u);
-  const uint32_t t0 = r0 | (r0 >> 4);
-  const uint32_t t1 = r1 | (r1 >> 4);
-  return __byte_perm(t0, t1, 0x6420) | ((w & 0x88888888u) ^ sx);
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ void requant_group(uint4 d, uint32_t sc, uint4& o,
@@ -104,31 +81,50 @@ __device__ __forceinline__ void requant_group(uint4 d, uint32_t sc, uint4& o,
     byte = 0xFFu;
     return;
   }
+  // Elements as exact f16 pairs (first half: words x, y; second: z, w).
+  uint32_t hx[4], hy[4], hz[4], hw[4];
+  e2m1x8_to_f16x8(d.x, hx);
+  e2m1x8_to_f16x8(d.y, hy);
+  e2m1x8_to_f16x8(d.z, hz);
+  e2m1x8_to_f16x8(d.w, hw);
+  // Largest |e2m1| of each half.
+  uint32_t m0 = hmax_abs2(hmax_abs2(hmax_abs2(hx[0], hx[1]), hmax_abs2(hx[2], hx[3])),
+                          hmax_abs2(hmax_abs2(hy[0], hy[1]), hmax_abs2(hy[2], hy[3])));
+  uint32_t m1 = hmax_abs2(hmax_abs2(hmax_abs2(hz[0], hz[1]), hmax_abs2(hz[2], hz[3])),
+                          hmax_abs2(hmax_abs2(hw[0], hw[1]), hmax_abs2(hw[2], hw[3])));
+  const float2 mm0 = __half22float2(*reinterpret_cast<__half2*>(&m0));
+  const float2 mm1 = __half22float2(*reinterpret_cast<__half2*>(&m1));
   const float2 s = e4m3x2_to_f32x2(sc);
-  const float a0 = fabsf(s.x), a1 = fabsf(s.y);
-  const float amax = fmaxf(e2m1_mag(max_mag16(d.x, d.y)) * a0,
-                           e2m1_mag(max_mag16(d.z, d.w)) * a1);
+  const float amax = fmaxf(fmaxf(fabsf(mm0.x), fabsf(mm0.y)) * fabsf(s.x),
+                           fmaxf(fabsf(mm1.x), fabsf(mm1.y)) * fabsf(s.y));
   int e = 0;
   if (amax > 0.0f) {
-    // amax = 1.f * 2^E; 6 * 2^(E-2) = 1.5 * 2^E covers f <= 1.5.
     const uint32_t bits = __float_as_uint(amax);
     const int E = static_cast<int>(bits >> 23) - 127;
     e = ((bits & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;
   }
   e = max(-126, min(127, e));
   byte = static_cast<uint32_t>(e + 127);
-  // |s| / 2^e: e is in [-13, 9] for any finite non-zero group, so the power
-  // of two is a normal float.
+  // s / 2^e per half as an f16 pair: exact, since e is in [-13, 9] for any
+  // finite non-zero group and s has at most four significant bits.  A half
+  // with nonzero codes has |s| / 2^e <= 12; an all-zero half may exceed f16
+  // range, so the factor is clamped to +-16 (its products stay +-0).
   const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-  uint32_t l0, h0, l1, h1;
-  build_lut(a0 * inv, l0, h0);
-  build_lut(a1 * inv, l1, h1);
-  const uint32_t sx0 = (sb0 & 0x80u) ? 0x88888888u : 0u;
-  const uint32_t sx1 = (sb1 & 0x80u) ? 0x88888888u : 0u;
-  o.x = remap8(d.x, l0, h0, sx0);
-  o.y = remap8(d.y, l0, h0, sx0);
-  o.z = remap8(d.z, l1, h1, sx1);
-  o.w = remap8(d.w, l1, h1, sx1);
+  const __half2 f = __floats2half2_rn(fminf(fmaxf(s.x * inv, -16.0f), 16.0f),
+                                      fminf(fmaxf(s.y * inv, -16.0f), 16.0f));
+  const uint32_t fb = *reinterpret_cast<const uint32_t*>(&f);
+  const uint32_t f0 = __byte_perm(fb, fb, 0x1010), f1 = __byte_perm(fb, fb, 0x3232);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    hx[i] = hmul2(hx[i], f0);
+    hy[i] = hmul2(hy[i], f0);
+    hz[i] = hmul2(hz[i], f1);
+    hw[i] = hmul2(hw[i], f1);
+  }
+  o.x = f16x8_to_e2m1x8(hx);
+  o.y = f16x8_to_e2m1x8(hy);
+  o.z = f16x8_to_e2m1x8(hz);
+  o.w = f16x8_to_e2m1x8(hw);
 }
 
 // Each thread takes kRqUnroll groups per iteration with all loads issued

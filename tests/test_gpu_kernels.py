@@ -51,6 +51,30 @@ def test_requant_every_code_and_scale(orc):
     assert fp4.last_device_error() == fp4.OK
 
 
+def test_requant_zero_half_beside_tiny_half(orc):
+    # One 16-half all +-0 codes under every finite scale, the other half
+    # tiny values under the smallest scales: the group exponent is then far
+    # below the zero half's scale (s / 2^e up to 448 * 2^13), which must
+    # still give +-0 codes with their signs kept.
+    n = FINITE_E4M3.size
+    g = np.random.default_rng(21)
+    codes = np.empty((n, 16), dtype=np.uint8)
+    codes[:, :8] = g.choice(np.array([0x00, 0x08, 0x80, 0x88], dtype=np.uint8),
+                            size=(n, 8))
+    codes[:, 8:] = g.integers(0, 256, size=(n, 8), dtype=np.uint8) & 0x99
+    scales = np.empty((n, 2), dtype=np.uint8)
+    scales[:, 0] = FINITE_E4M3
+    scales[:, 1] = g.choice(np.array([0x01, 0x02, 0x81, 0x09], dtype=np.uint8), size=n)
+    # the same with the halves swapped
+    codes = np.concatenate([codes, np.concatenate([codes[:, 8:], codes[:, :8]], 1)])
+    scales = np.concatenate([scales, scales[:, ::-1]])
+    ref_c, ref_s = orc.requant(codes, scales)
+    got_c, got_s = gpu_requant(codes, scales)
+    np.testing.assert_array_equal(got_s, ref_s)
+    np.testing.assert_array_equal(got_c, ref_c)
+    assert fp4.last_device_error() == fp4.OK
+
+
 def test_requant_nan_scale(orc):
     codes = synth.random_bytes((8, 64), 13)
     scales = np.full((8, 8), 0x38, dtype=np.uint8)
