@@ -192,7 +192,7 @@ class MoeRun:
 
     @property
     def launches_per_step(self) -> int:
-        return 8 if self.fp8 else 6
+        return 9 if self.fp8 else 7
 
     def timed(self, steps, warmup, clocks=None):
         torch, fp4 = self.torch, self.fp4

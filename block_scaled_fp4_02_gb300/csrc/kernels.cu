@@ -396,16 +396,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(
 // Stable scatter: within block b (tokens [32b, 32b+32)), the rank of pair p
 // among the block's pairs of the same expert is the number of lower-indexed
 // pairs of that expert: earlier warps (per-warp counts in shared memory) plus
-// lower lanes of this warp (match mask).  Then the block copies each pair's
-// activation row into its expert-major slot.
+// lower lanes of this warp (match mask).
 __global__ void __launch_bounds__(512) scatter_kernel(
     const int32_t* __restrict__ ids, int T, int E, int k,
     const int32_t* __restrict__ base, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv, const void* __restrict__ x,
-    const uint8_t* __restrict__ xs, int K, int act_mode,
-    uint16_t* __restrict__ xperm) {
+    int32_t* __restrict__ inv) {
   extern __shared__ int wcnt[];   // [16 warps][E]
-  __shared__ int spos[kTokPerBlk * kMaxTopK];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t P = static_cast<int64_t>(T) * k;
   const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kTokPerBlk * k;
@@ -424,24 +420,27 @@ __global__ void __launch_bounds__(512) scatter_kernel(
     const int pos = base[static_cast<int64_t>(blockIdx.x) * E + e] + pre + rank;
     perm[pos] = static_cast<int32_t>(p0 + tid);
     inv[p0 + tid] = pos;
-    spos[tid] = pos;
   }
-  if (xperm == nullptr) return;
-  __syncthreads();
-  for (int i = warp; i < np; i += 16) {
-    const int64_t t = (p0 + i) / k;
-    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<int64_t>(spos[i]) * K);
+}
+
+// Activation gather: row p of the pair list goes to expert-major slot inv[p]
+// (one block per row, grid-stride over rows), as bf16; FP8 inputs are
+// dequantized exactly on the way.
+__global__ void __launch_bounds__(256) gather_kernel(
+    const int32_t* __restrict__ inv, int64_t P, int k, const void* __restrict__ x,
+    const uint8_t* __restrict__ xs, int K, int act_mode, uint16_t* __restrict__ xperm) {
+  for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
+    const int64_t t = p / k;
+    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<int64_t>(inv[p]) * K);
     if (act_mode == FP4MOE_ACT_BF16) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const uint16_t*>(x) + t * K);
-      for (int c = lane; c < K / 8; c += 32) dst[c] = src[c];
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + t * K);
+      for (int c = threadIdx.x; c < K / 8; c += blockDim.x) dst[c] = __ldg(src + c);
     } else {
       // FP8: bf16(e4m3 * 2^(xs - 127)), exact for scaled values in the
       // bf16 normal range.
-      const uint2* src = reinterpret_cast<const uint2*>(
-          static_cast<const uint8_t*>(x) + t * K);
+      const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(x) + t * K);
       const uint8_t* srow = xs + t * (K / 32);
-      for (int c = lane; c < K / 8; c += 32) {
+      for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
         const uint2 q = src[c];
         const uint32_t sb = srow[c / 4];
         const float sc = (sb == 0)     ? __uint_as_float(0x00400000u)
@@ -449,8 +448,7 @@ __global__ void __launch_bounds__(512) scatter_kernel(
                                        : __uint_as_float(sb << 23);
         const float2 a = e4m3x2_to_f32x2(q.x), b = e4m3x2_to_f32x2(q.x >> 16);
         const float2 c2 = e4m3x2_to_f32x2(q.y), d2 = e4m3x2_to_f32x2(q.y >> 16);
-        dst[c] = make_uint4(pack_bf16x2(a.x * sc, a.y * sc),
-                            pack_bf16x2(b.x * sc, b.y * sc),
+        dst[c] = make_uint4(pack_bf16x2(a.x * sc, a.y * sc), pack_bf16x2(b.x * sc, b.y * sc),
                             pack_bf16x2(c2.x * sc, c2.y * sc),
                             pack_bf16x2(d2.x * sc, d2.y * sc));
       }
@@ -718,8 +716,12 @@ cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv, x, xs,
-                                          K, act_mode, xperm);
+  scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || xperm == nullptr) return e;
+  const int64_t P = static_cast<int64_t>(T) * k;
+  const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
+  gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm);
   return cudaGetLastError();
 }
 
