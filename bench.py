@@ -40,6 +40,11 @@ METRIC = ("MoE-layer tokens/s, TFLOP/s & weight GB/s vs GB300 roofline; "
           "requant GB/s")
 WORKLOADS = {"prefill": synth.PREFILL, "decode": synth.DECODE,
              "decode_skew": synth.DECODE_SKEW, "fp8": synth.FP8,
+             # FP8 activations over the group16 weights without the requant
+             "fp8_g16": synth.MoeConfig(
+                 "fp8xfp4_group16_E128_K7168_I2048_T4096_k8", 128, 7168, 2048,
+                 4096, 8, act="fp8", weight_seed=1005, input_seed=2005,
+                 keep_group16=True),
              "tiny": synth.TINY,
              # small cases of the same kernels for ncu captures (inputs larger
              # than L2, a few GB on the device at most)
@@ -61,7 +66,7 @@ def parse_args():
     ap.add_argument("--impl", default="fp4moe",
                     choices=["fp4moe", "reference"])
     ap.add_argument("--workload", default="prefill", choices=sorted(WORKLOADS))
-    ap.add_argument("--extra", default="decode,decode_skew,fp8,requant",
+    ap.add_argument("--extra", default="decode,decode_skew,fp8,fp8_g16,requant",
                     help="comma list of extra workloads, or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -155,6 +160,8 @@ class MoeRun:
         self.cfg, self.fp4, self.torch = cfg, fp4, torch
         self.fp8 = cfg.act == "fp8"
         act = fp4.ACT_FP8 if self.fp8 else fp4.ACT_BF16
+        if cfg.keep_group16:
+            act |= fp4.FLAG_KEEP_GROUP16
         dev = {k: torch.from_numpy(v).cuda() for k, v in weights.items()}
         self.packed = fp4.prepare_weights(
             dev["w13"], dev["w13_s"], dev["w13_gs"], dev["w2"], dev["w2_s"],
@@ -488,7 +495,8 @@ def main():
             continue
         c = WORKLOADS[name]
         key = (c.E, c.K, c.I, c.weight_seed)
-        if key in shared and shared[key].cfg.act == c.act:
+        if (key in shared and shared[key].cfg.act == c.act and
+                shared[key].cfg.keep_group16 == c.keep_group16):
             # same weights: reuse the packed set, new activations/routing
             base = shared[key]
             r = MoeRun.__new__(MoeRun)

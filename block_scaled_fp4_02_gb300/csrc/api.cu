@@ -253,7 +253,9 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
   *out = nullptr;
   const int mode = act_mode & 0xFF;
   const bool no_requant = (act_mode & FP4MOE_FLAG_NO_REQUANT) != 0;
-  if ((act_mode & ~(0xFF | FP4MOE_FLAG_NO_REQUANT)) != 0) return FP4MOE_ERR_INVALID_ARG;
+  const bool keep16 = (act_mode & FP4MOE_FLAG_KEEP_GROUP16) != 0;
+  if ((act_mode & ~(0xFF | FP4MOE_FLAG_NO_REQUANT | FP4MOE_FLAG_KEEP_GROUP16)) != 0)
+    return FP4MOE_ERR_INVALID_ARG;
   if (mode != FP4MOE_ACT_BF16 && mode != FP4MOE_ACT_FP8) return FP4MOE_ERR_INVALID_ARG;
   if (gran_k != 16 && gran_k != 32) return FP4MOE_ERR_INVALID_ARG;
   if (w13_layout != FP4MOE_W13_GATE_UP && w13_layout != FP4MOE_W13_UP_GATE)
@@ -262,7 +264,9 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
     return FP4MOE_ERR_INVALID_ARG;
   if (!w13 || !w13_s || !w13_gs || !w2 || !w2_s || !w2_gs) return FP4MOE_ERR_INVALID_ARG;
   if (!aligned(w13, 16) || !aligned(w2, 16)) return FP4MOE_ERR_INVALID_ARG;
-  const bool requant = (mode == FP4MOE_ACT_FP8 && gran_k == 16);
+  // FP8 over group16: lossy requant to group32, unless the exact group16
+  // conversion is asked for (KEEP_GROUP16) or refused (NO_REQUANT).
+  const bool requant = (mode == FP4MOE_ACT_FP8 && gran_k == 16 && !keep16);
   if (requant && no_requant) return FP4MOE_ERR_UNSUPPORTED;
   const int g = requant ? 32 : gran_k;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -58,6 +58,14 @@ enum fp4moe_act_mode { FP4MOE_ACT_BF16 = 0, FP4MOE_ACT_FP8 = 1 };
  * FP8 + gran_k 16 + this flag -> UNSUPPORTED. */
 #define FP4MOE_FLAG_NO_REQUANT 0x100
 
+/* Flag OR-ed into act_mode of fp4moe_prepare_weights: FP8 activations over
+ * group16 (E4M3-scaled) weights without the lossy requant.  The GEMM converts
+ * e2m1 * E4M3 exactly, as in the bf16 path, so the result is the exact
+ * group16 product (the group16 notes page's "remaining kernel work" of a
+ * software group16 path in the FP8 kernel).  Takes precedence over
+ * FP4MOE_FLAG_NO_REQUANT; no effect unless act_mode is FP8 and gran_k 16. */
+#define FP4MOE_FLAG_KEEP_GROUP16 0x200
+
 /* Opaque prepared weights.  Owned by the library until fp4moe_free_packed. */
 typedef struct fp4moe_packed fp4moe_packed;
 
@@ -113,8 +121,9 @@ int fp4moe_act_quant(const void* x_bf16, int64_t T, int64_t K, uint8_t* xq,
  *   w13 [E, 2I, K/2] codes, w13_s [E, 2I, K/gran_k], w13_gs [E] FP32,
  *   w2  [E, K, I/2]  codes, w2_s  [E, K, I/gran_k],  w2_gs  [E] FP32.
  * gran_k 16 -> E4M3 scales, 32 -> UE8M0 scales.  act_mode FP4MOE_ACT_BF16
- * or FP4MOE_ACT_FP8, optionally OR FP4MOE_FLAG_NO_REQUANT.  With FP8 and
- * gran_k 16 the weights are requantized to group32 first (lossy, as above).
+ * or FP4MOE_ACT_FP8, optionally OR FP4MOE_FLAG_NO_REQUANT or
+ * FP4MOE_FLAG_KEEP_GROUP16.  With FP8 and gran_k 16 the weights are
+ * requantized to group32 first (lossy, as above) unless KEEP_GROUP16 is set.
  * Requires K % 128 == 0, I % 128 == 0, E >= 1.
  * SYNCHRONOUS: allocates device memory for the packed weights, runs the
  * packing kernels on `stream`, synchronises it, and returns INVALID_ARG if a

@@ -45,6 +45,7 @@ class MoeConfig:
     weight_seed: int = 0
     input_seed: int = 0
     w13_layout: int = 0      # 0 = gate_up ("w31"), 1 = up_gate ("w13")
+    keep_group16: bool = False   # FP8 over the group16 weights as they are
 
     @property
     def pairs(self) -> int:

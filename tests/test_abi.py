@@ -81,7 +81,7 @@ def _prepare(lib, **kw):
 
 def test_prepare_argument_checks(lib):
     for kw in [dict(gran=8), dict(layout=2), dict(act=3), dict(K=192),
-               dict(I=64), dict(E=0), dict(w2=None), dict(act=0x200)]:
+               dict(I=64), dict(E=0), dict(w2=None), dict(act=0x400)]:
         rc, out = _prepare(lib, **kw)
         assert rc == fp4.ERR_INVALID_ARG, kw
         assert not out.value
@@ -89,6 +89,10 @@ def test_prepare_argument_checks(lib):
     # like the fused-compute capability gate for recipe (1,1,16).
     rc, out = _prepare(lib, act=fp4.ACT_FP8 | fp4.FLAG_NO_REQUANT, gran=16)
     assert rc == fp4.ERR_UNSUPPORTED and not out.value
+    # The exact-group16 flag is a known bit: a bad shape is still reported
+    # as such (these checks never reach the device).
+    rc, out = _prepare(lib, act=fp4.ACT_FP8 | fp4.FLAG_KEEP_GROUP16, gran=16, K=192)
+    assert rc == fp4.ERR_INVALID_ARG and not out.value
 
 
 def test_moe_argument_checks(lib):

@@ -87,6 +87,7 @@ def check_against_oracle(orc, cfg, w, acts, p, y, ws, tokens, layout=0,
 # ------------------------------------------------------------------ layout
 
 @pytest.mark.parametrize("gran,act", [(16, fp4.ACT_BF16), (16, fp4.ACT_FP8),
+                                      (16, fp4.ACT_FP8 | fp4.FLAG_KEEP_GROUP16),
                                       (32, fp4.ACT_BF16)])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_prepare_layout_roundtrip(orc, gran, act, layout):
@@ -97,7 +98,7 @@ def test_prepare_layout_roundtrip(orc, gran, act, layout):
     p = prepare(w, gran=gran, layout=layout, act=act)
     bufs = p.buffers()
     d = p.desc
-    if act == fp4.ACT_FP8 and gran == 16:
+    if act == fp4.ACT_FP8 and gran == 16:   # lossy requant to group32
         ref_w = requant_weights_oracle(orc, w, E, K, I)
         rg = 32
     else:
@@ -152,6 +153,51 @@ def test_moe_group32_weights_bf16_activations(orc):
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
     check_against_oracle(orc, cfg, w32, acts, p, y, ws, range(cfg.T), gran=32,
                          what="group32 bf16")
+
+
+def _fp8_group16_oracle(orc, cfg, w, acts, tokens):
+    xq, xs = orc.act_quant(acts["x_bf16"])
+    return orc.moe_rows(tokens, **w, gran=16, w13_layout=0, act_mode=1,
+                        top_k=cfg.top_k, logits=acts["logits"], xq=xq, xs=xs,
+                        return_h=True)
+
+
+def test_moe_fp8_keep_group16(orc):
+    # FP8 activations over group16 weights without the lossy requant: the
+    # oracle runs the group16 weights as they are.
+    cfg = synth.SMALL_FP8
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w, act=fp4.ACT_FP8 | fp4.FLAG_KEEP_GROUP16)
+    assert p.desc.gran_k == 16 and p.desc.act_mode == fp4.ACT_FP8
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_FP8)
+    tokens = list(range(cfg.T))
+    ref_y, ref_h, aux = _fp8_group16_oracle(orc, cfg, w, acts, tokens)
+    check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, aux, w, 16, 1,
+              acts["logits"], "fp8 keep group16")
+
+
+def test_fp8_group16_accuracy_gap(orc, record_property):
+    # Against the exact FP64 result over the group16 weights, the kept
+    # group16 path errs only by its roundings; the requant path adds the
+    # group32 re-rounding of the weights.  Relative RMS errors are recorded.
+    cfg = synth.SMALL_FP8
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    tokens = list(range(cfg.T))
+    ref_y = _fp8_group16_oracle(orc, cfg, w, acts, tokens)[0].reshape(cfg.T, cfg.K)
+    errs = {}
+    for name, mode in (("keep_group16", fp4.ACT_FP8 | fp4.FLAG_KEEP_GROUP16),
+                       ("requant_group32", fp4.ACT_FP8)):
+        p = prepare(w, act=mode)
+        y, _ = gpu_forward(p, acts, cfg.top_k, fp4.ACT_FP8)
+        d = y.float().cpu().numpy().astype(np.float64) - ref_y
+        errs[name] = float(np.sqrt((d ** 2).mean() / (ref_y ** 2).mean()))
+        record_property(name + "_rel_rms", errs[name])
+        del p
+    print("fp8 relative RMS error vs exact group16:", errs)
+    assert errs["keep_group16"] < 2.0 ** -7
+    assert errs["keep_group16"] < errs["requant_group32"]
 
 
 @pytest.mark.parametrize("T", [1, 2, 17, 300])
