@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "FP4MoEError", "ACT_BF16", "ACT_FP8", "W13_GATE_UP", "W13_UP_GATE",
-    "FLAG_NO_REQUANT", "FLAG_KEEP_GROUP16", "load", "build", "exported_symbols",
+    "FLAG_NO_REQUANT", "FLAG_KEEP_GROUP16", "FLAG_GS_INVERTED", "load", "build", "exported_symbols",
     "requant_fp4_gran_k", "act_quant", "route_debug", "route_workspace_size",
     "prepare_weights", "PackedWeights", "moe_workspace_size", "moe_forward",
     "moe_workspace_size_host", "moe_forward_host", "status_string",
@@ -32,6 +32,7 @@ W13_GATE_UP, W13_UP_GATE = 0, 1
 ACT_BF16, ACT_FP8 = 0, 1
 FLAG_NO_REQUANT = 0x100
 FLAG_KEEP_GROUP16 = 0x200
+FLAG_GS_INVERTED = 0x400
 
 _HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(
     __file__))), "include", "fp4moe.h")

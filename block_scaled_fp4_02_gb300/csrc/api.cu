@@ -254,7 +254,9 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
   const int mode = act_mode & 0xFF;
   const bool no_requant = (act_mode & FP4MOE_FLAG_NO_REQUANT) != 0;
   const bool keep16 = (act_mode & FP4MOE_FLAG_KEEP_GROUP16) != 0;
-  if ((act_mode & ~(0xFF | FP4MOE_FLAG_NO_REQUANT | FP4MOE_FLAG_KEEP_GROUP16)) != 0)
+  const bool gs_inv = (act_mode & FP4MOE_FLAG_GS_INVERTED) != 0;
+  if ((act_mode & ~(0xFF | FP4MOE_FLAG_NO_REQUANT | FP4MOE_FLAG_KEEP_GROUP16 |
+                    FP4MOE_FLAG_GS_INVERTED)) != 0)
     return FP4MOE_ERR_INVALID_ARG;
   if (mode != FP4MOE_ACT_BF16 && mode != FP4MOE_ACT_FP8) return FP4MOE_ERR_INVALID_ARG;
   if (gran_k != 16 && gran_k != 32) return FP4MOE_ERR_INVALID_ARG;
@@ -333,8 +335,8 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
   if (e == cudaSuccess)
     e = launch_pack(c2, s2, E, static_cast<int>(n2), I, g, false, 0, bmax + E, p->w2,
                     err, st);
-  if (e == cudaSuccess) e = launch_alpha(w13_gs, bmax, E, g, p->alpha, st);
-  if (e == cudaSuccess) e = launch_alpha(w2_gs, bmax + E, E, g, p->alpha + E, st);
+  if (e == cudaSuccess) e = launch_alpha(w13_gs, bmax, E, g, gs_inv, p->alpha, st);
+  if (e == cudaSuccess) e = launch_alpha(w2_gs, bmax + E, E, g, gs_inv, p->alpha + E, st);
   if (e != cudaSuccess) return fail(FP4MOE_ERR_CUDA);
   if (cudaStreamSynchronize(st) != cudaSuccess) return fail(FP4MOE_ERR_CUDA);
   int h_err = 0;

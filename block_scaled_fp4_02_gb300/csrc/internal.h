@@ -65,8 +65,10 @@ cudaError_t launch_pack(const uint8_t* w, const uint8_t* s, int E, int N,
                         int Kd, int gran, bool gated, int layout,
                         const int32_t* bmax, uint8_t* out, int* err,
                         cudaStream_t st);
+// alpha = gs (or 1 / gs when the global scales are stored inverted) times
+// the power of two that the packed scale codes leave out.
 cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E,
-                         int gran, float* alpha, cudaStream_t st);
+                         int gran, bool inverted, float* alpha, cudaStream_t st);
 
 // S5 / S6: grouped GEMM over packed weights.
 struct GemmArgs {

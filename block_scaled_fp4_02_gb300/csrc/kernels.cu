@@ -632,10 +632,11 @@ __global__ void __launch_bounds__(128) pack_kernel(
 
 __global__ void alpha_kernel(const float* __restrict__ gs,
                              const int32_t* __restrict__ bmax, int E, int gran,
-                             float* __restrict__ alpha) {
+                             int inverted, float* __restrict__ alpha) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
-  alpha[e] = (gran == 16) ? gs[e] * 128.0f : ldexpf(gs[e], bmax[e] - 128);
+  const float g = inverted ? 1.0f / gs[e] : gs[e];   // IEEE division
+  alpha[e] = (gran == 16) ? g * 128.0f : ldexpf(g, bmax[e] - 128);
 }
 
 }  // namespace
@@ -752,9 +753,9 @@ cudaError_t launch_pack(const uint8_t* w, const uint8_t* s, int E, int N,
   return cudaGetLastError();
 }
 
-cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E, int gran,
+cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E, int gran, bool inverted,
                          float* alpha, cudaStream_t st) {
-  alpha_kernel<<<(E + 255) / 256, 256, 0, st>>>(gs, bmax, E, gran, alpha);
+  alpha_kernel<<<(E + 255) / 256, 256, 0, st>>>(gs, bmax, E, gran, inverted ? 1 : 0, alpha);
   return cudaGetLastError();
 }
 

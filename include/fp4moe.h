@@ -66,6 +66,11 @@ enum fp4moe_act_mode { FP4MOE_ACT_BF16 = 0, FP4MOE_ACT_FP8 = 1 };
  * FP4MOE_FLAG_NO_REQUANT; no effect unless act_mode is FP8 and gran_k 16. */
 #define FP4MOE_FLAG_KEEP_GROUP16 0x200
 
+/* Flag OR-ed into act_mode of fp4moe_prepare_weights: w13_gs and w2_gs are
+ * stored inverted (the compressed-tensors checkpoint convention of the
+ * prepare page); the scale applied is 1 / gs, an FP32 division. */
+#define FP4MOE_FLAG_GS_INVERTED 0x400
+
 /* Opaque prepared weights.  Owned by the library until fp4moe_free_packed. */
 typedef struct fp4moe_packed fp4moe_packed;
 
@@ -122,7 +127,7 @@ int fp4moe_act_quant(const void* x_bf16, int64_t T, int64_t K, uint8_t* xq,
  *   w2  [E, K, I/2]  codes, w2_s  [E, K, I/gran_k],  w2_gs  [E] FP32.
  * gran_k 16 -> E4M3 scales, 32 -> UE8M0 scales.  act_mode FP4MOE_ACT_BF16
  * or FP4MOE_ACT_FP8, optionally OR FP4MOE_FLAG_NO_REQUANT or
- * FP4MOE_FLAG_KEEP_GROUP16.  With FP8 and gran_k 16 the weights are
+ * FP4MOE_FLAG_KEEP_GROUP16, and FP4MOE_FLAG_GS_INVERTED.  With FP8 and gran_k 16 the weights are
  * requantized to group32 first (lossy, as above) unless KEEP_GROUP16 is set.
  * Requires K % 128 == 0, I % 128 == 0, E >= 1.
  * SYNCHRONOUS: allocates device memory for the packed weights, runs the

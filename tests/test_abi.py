@@ -81,7 +81,7 @@ def _prepare(lib, **kw):
 
 def test_prepare_argument_checks(lib):
     for kw in [dict(gran=8), dict(layout=2), dict(act=3), dict(K=192),
-               dict(I=64), dict(E=0), dict(w2=None), dict(act=0x400)]:
+               dict(I=64), dict(E=0), dict(w2=None), dict(act=0x800)]:
         rc, out = _prepare(lib, **kw)
         assert rc == fp4.ERR_INVALID_ARG, kw
         assert not out.value

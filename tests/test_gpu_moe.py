@@ -200,6 +200,29 @@ def test_fp8_group16_accuracy_gap(orc, record_property):
     assert errs["keep_group16"] < errs["requant_group32"]
 
 
+def test_moe_inverted_global_scales():
+    # Compressed-tensors checkpoints store 1/gs: with the flag, prepare takes
+    # the reciprocal (FP32 division), so the layer equals the one prepared
+    # from the reciprocal computed on the host, bit for bit.
+    cfg = synth.SMALL_DECODE
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    inv = dict(w)
+    for k in ("w13_gs", "w2_gs"):
+        inv[k] = (np.float32(1.0) / w[k].astype(np.float32)).astype(np.float32)
+    direct = dict(w)
+    for k in ("w13_gs", "w2_gs"):
+        direct[k] = (np.float32(1.0) / inv[k]).astype(np.float32)
+    p_inv = prepare(inv, act=fp4.ACT_BF16 | fp4.FLAG_GS_INVERTED)
+    p_dir = prepare(direct)
+    y_inv, _ = gpu_forward(p_inv, acts, cfg.top_k, fp4.ACT_BF16)
+    y_dir, _ = gpu_forward(p_dir, acts, cfg.top_k, fp4.ACT_BF16)
+    assert torch.equal(y_inv.view(torch.int16), y_dir.view(torch.int16))
+    a_inv = p_inv.buffers()["alpha13"].numpy()
+    a_dir = p_dir.buffers()["alpha13"].numpy()
+    np.testing.assert_array_equal(a_inv, a_dir)
+
+
 @pytest.mark.parametrize("T", [1, 2, 17, 300])
 def test_moe_token_counts(orc, T):
     base = synth.SMALL_DECODE
