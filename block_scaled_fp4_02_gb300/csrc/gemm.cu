@@ -57,17 +57,19 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int NT>
 struct Cfg {
-  static constexpr bool kATmem = NT <= 64;         // A stages in TMEM
+  static_assert(NT == 32 || NT == 256, "the two variants of the kernel");
+  static constexpr bool kATmem = NT == 32;         // A stages in TMEM
   static constexpr int kMT = kATmem ? 1 : 2;       // weight tiles per unit
   // One thread issues a tcgen05.mma about every 55 cycles whatever its size,
   // while the tensor pipe takes a short (N <= 32, A in TMEM) one every ~14:
-  // with A in TMEM four warps issue, one per SM sub-partition (warp % 4).
-  // With A in shared memory two MMA warps each own one weight tile (all K
-  // steps); with A in TMEM the MMA warps split the K steps.
-  static constexpr int kMmaWarps = !kATmem ? 2 : (NT <= 32 ? 4 : 2);
+  // with A in TMEM four warps issue, one per SM sub-partition (warp % 4),
+  // and split the K steps; with A in shared memory two MMA warps each own
+  // one weight tile (all K steps).
+  static constexpr int kMmaWarps = kATmem ? 4 : 2;
   static constexpr int kEpiWarps = kATmem ? 4 : 8;
-  // First MMA warp: warp 1 (shared-memory A) or the four warps after the
-  // epilogue (TMEM A; warp 1 then only allocates TMEM).
+  // The warps after the epilogue: TMEM A, the four MMA warps and then two
+  // activation producers; shared-memory A, the MMA warp of tile 1 (warp 1
+  // issues tile 0).
   static constexpr int kWarpMmaX0 = kWarpEpi0 + kEpiWarps;
   static constexpr int kWarpBX0 = kWarpMmaX0 + kMmaWarps;   // extra B producers
   static constexpr int kExtraB = kATmem ? 2 : 0;
@@ -357,8 +359,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) record_error(a.err, FP4MOE_ERR_TIMEOUT);
     }
-  } else if (warp == kWarpMma) {
-    // Not reached: with TMEM A warp 1 is an activation producer.
   } else if (warp < kWarpEpi0 && C::kATmem) {
     // ------------------------------------------- dequant, A in TMEM (NT=32)
     // Group g (four warps) takes the K steps n = g (mod 4); warp q of the
@@ -437,16 +437,14 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
     const uint32_t a_row_off = (r >> 3) * 1024u + (r & 7) * 128u;
     const uint32_t sw = r & 7, cb = 4 * khalf;
-    // MT = 2: group g fills weight tile g of every step; MT = 1: the groups
-    // take alternate steps into the single tile.
-    const int tile = (MT > 1) ? grp : 0;
+    // Group g fills weight tile g of every step (nothing to load when the
+    // unit's second block does not exist: odd block count).
+    const int tile = grp;
     uint32_t n = 0;                   // global K-step counter of this CTA
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const bool live = (MT == 1) ||
-                        (decode_unit(a, nbu, MT, tab_cs, tab_os, u).nb + tile < a.nblocks);
+      const bool live = decode_unit(a, nbu, MT, tab_cs, tab_os, u).nb + tile < a.nblocks;
       for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
-        if (MT == 1 && static_cast<int>(n % kDqGroups) != grp) continue;
         const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SAa);
         const uint32_t phf = (n / SF) & 1u, pha = (n / SAa) & 1u;
         uint4 w0, w1, w2, w3;
