@@ -317,3 +317,18 @@ def test_moe_full_size_sampled(orc, cfg, n):
     toks = _sample_tokens(cfg.T, n, 99)
     check_against_oracle(orc, cfg, w, acts, p, y, ws, toks)
     p.free()
+
+
+def test_moe_full_size_fp8_keep_group16(orc):
+    """The FP8 workload with its group16 weights kept (no requant), sampled
+    rows against the oracle over the group16 weights."""
+    cfg = synth.FP8
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w, act=fp4.ACT_FP8 | fp4.FLAG_KEEP_GROUP16)
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_FP8)
+    toks = _sample_tokens(cfg.T, 24, 98)
+    ref_y, ref_h, aux = _fp8_group16_oracle(orc, cfg, w, acts, toks)
+    check_moe(orc, fp4, cfg, p, y, ws, toks, ref_y, ref_h, aux, w, 16, 1,
+              acts["logits"], "fp8 keep group16, full size")
+    p.free()
