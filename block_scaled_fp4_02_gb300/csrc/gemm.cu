@@ -14,10 +14,11 @@
 //   NT = 32 (decode): MT = 1; A lives in TMEM.  One thread issues an
 //     asynchronous instruction (tcgen05.mma, a TMA copy) only every ~100
 //     cycles or more, far below what the tensor and TMA units take, so the
-//     issue is spread: four MMA warps take K steps n = 0..3 (mod 4) into
-//     their own accumulators (summed in the epilogue, double-buffered), four
-//     threads load the activation rows (steps n = 0..3 (mod 4)), and each
-//     weight copy brings two K steps.
+//     issue is spread and amortized: the unit of hand-off is a pair of K
+//     steps (128 wide: one weight copy, one TMEM A stage of 64 columns, eight
+//     MMAs); four MMA warps take pairs m = 0..3 (mod 4) into their own
+//     accumulators (summed in the epilogue, double-buffered), and four
+//     threads load the activation rows (steps n = 0..3 (mod 4)).
 // Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
 //                 (MT per K step, or two K steps with NT = 32) into a ring of
@@ -32,7 +33,7 @@
 //   warps 3..18 : dequantizers: NT = 256, two groups of eight (warp w owns
 //                 rows 32*(w%4).. and one 32-wide K half; group g fills
 //                 weight tile g of every step); NT = 32, four groups of four
-//                 (whole K step; group g takes steps n = g (mod 4));
+//                 (group g converts the pairs m = g (mod 4) into A stage g);
 //   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
 //                 reading the TMEM accumulators; then NT = 256 has the MMA
 //                 warp of tile 1, NT = 32 its four MMA warps (one per SM
@@ -79,7 +80,7 @@ struct Cfg {
   // memory or TMEM), B (activation rows, from L2 by TMA).
   static constexpr int kStepsPerF = kATmem ? 2 : 1;  // K steps per F stage
   static constexpr int kSF = kATmem ? 12 : 6;
-  static constexpr int kSAa = kATmem ? 8 : 2;      // TMEM A: 8 x 32 columns
+  static constexpr int kSAa = kATmem ? 4 : 2;      // TMEM A: 4 x 64 columns (two K tiles)
   static constexpr int kSB = kATmem ? 8 : 3;
   static constexpr uint32_t kFStage = kFBytes * kMT * kStepsPerF;
   static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
@@ -95,7 +96,7 @@ struct Cfg {
   // two groups of eight (row quarter x K half) that fill one tile each.
   static constexpr int kDqPerStage = kATmem ? 4 : kDqGroups * kDqWarps;
   // F stages are released by both groups whose steps they hold.
-  static constexpr int kDqPerF = kATmem ? 8 : kDqGroups * kDqWarps;
+  static constexpr int kDqPerF = kATmem ? 4 : kDqGroups * kDqWarps;
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = kAOff + kAStage * kSAa;
   static constexpr uint32_t kFOff = kBOff + kBStage * kSB;
@@ -107,9 +108,9 @@ struct Cfg {
   static constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
-                          kATmemCol + 32 * kSAa <= kTmemCols)
+                          kATmemCol + 64 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
-  static_assert(!kATmem || (kSAa == kSB && kSF % 2 == 0 && kSAa % 4 == 0),
+  static_assert(!kATmem || (kSB == 2 * kSAa && kSF % 4 == 0 && kSAa == 4),
                 "TMEM A rings: shared A/B release, four dequant groups");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
@@ -281,7 +282,13 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           if (static_cast<int>(n % nprod) != bp) continue;
           const int s = static_cast<int>(n % SB);
           const uint32_t ph = (n / SB) & 1u;
-          if (!mbar_wait(C::kATmem ? emptyA(s) : emptyB(s), ph ^ 1u)) { ok = false; break; }
+          // TMEM A: the stage is free once the MMAs of the pair (n / 2) that
+          // last used it completed (released with that pair's A stage).
+          const bool fr = C::kATmem
+              ? mbar_wait(emptyA(static_cast<int>((n >> 1) % SAa)),
+                          (((n >> 1) / SAa) & 1u) ^ 1u)
+              : mbar_wait(emptyB(s), ph ^ 1u);
+          if (!fr) { ok = false; break; }
           mbar_arrive_expect_tx(fullB(s), nbox * kBoxBytes);
           const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
           // Rows past the chunk (up to the box) are loaded but not used;
@@ -300,8 +307,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   } else if (C::kATmem ? warp >= C::kWarpMmaX0
                         : (warp == kWarpMma || warp == C::kWarpMmaX0)) {
     // ---------------------------------------------------------------- MMA
-    // TMEM A: warp mi takes K steps n % kMmaWarps == mi; shared-memory A:
-    // warp mi issues the MMAs of weight tile mi in every step.
+    // TMEM A: warp mi takes the pairs of K steps m = n / 2 with
+    // m % kMmaWarps == mi; shared-memory A: warp mi issues the MMAs of weight
+    // tile mi in every step.
     const int mi = C::kATmem ? warp - C::kWarpMmaX0 : (warp == kWarpMma ? 0 : 1);
     if (lane == 0) {
       int buf = 0;
@@ -319,10 +327,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         if (!mbar_wait(accEmpty(buf), acc_ph ^ 1u)) { ok = false; break; }
         tc_fence_after();
         uint32_t acc = 0;
-        for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
-          if (C::kATmem && static_cast<int>(n % C::kMmaWarps) != mi) continue;
-          const int sa = static_cast<int>(n % SAa), sb = static_cast<int>(n % SB);
-          if (!mbar_wait(fullB(sb), (n / SB) & 1u) || !mbar_wait(aready(sa), (n / SAa) & 1u)) {
+        for (int ks = 0; ks < a.ksteps; ks += (C::kATmem ? 2 : 1), n += (C::kATmem ? 2 : 1)) {
+          // TMEM A: pair m = n / 2 of K tiles, taken by MMA warp m % 4.
+          const uint32_t m = n >> 1;
+          if (C::kATmem && static_cast<int>(m % C::kMmaWarps) != mi) continue;
+          const int sa = static_cast<int>(C::kATmem ? m % SAa : n % SAa);
+          const uint32_t pa = C::kATmem ? (m / SAa) & 1u : (n / SAa) & 1u;
+          const int sb = static_cast<int>(n % SB);
+          if (!mbar_wait(fullB(sb), (n / SB) & 1u) ||
+              (C::kATmem && !mbar_wait(fullB((sb + 1) % SB), ((n + 1) / SB) & 1u)) ||
+              !mbar_wait(aready(sa), pa)) {
             ok = false;
             break;
           }
@@ -331,12 +345,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           // (2 in the descriptor's 16-byte address units).
           const uint64_t bd = bdesc0 + static_cast<uint64_t>((sb * C::kBStage) >> 4);
           if (C::kATmem) {
-            const uint32_t at = tmem + C::kATmemCol + sa * 32u;
+            const uint32_t at = tmem + C::kATmemCol + sa * 64u;
+            const uint64_t bd1 = bdesc0 + static_cast<uint64_t>((((sb + 1) % SB) * C::kBStage) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
               umma_f16_ta(d_tmem, at + kk * 8u, bd + 2u * kk, idesc, acc);
               acc = 1u;
             }
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk)
+              umma_f16_ta(d_tmem, at + 32u + kk * 8u, bd1 + 2u * kk, idesc, 1u);
           } else if (mi < tiles) {
             // Tile mi -> accumulator columns 256 mi (d_tmem).
             const uint64_t ad = adesc0 + static_cast<uint64_t>((sa * C::kAStage) >> 4) +
@@ -361,67 +379,66 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     }
   } else if (warp < kWarpEpi0 && C::kATmem) {
     // ------------------------------------------- dequant, A in TMEM (NT=32)
-    // Group g (four warps) takes the K steps n = g (mod 4); warp q of the
-    // group dequantizes rows 32q.. over the whole 64-wide step into TMEM
-    // lanes 32q.. (the lane quarter its warp may write).
+    // Group g (four warps) takes the pairs of K tiles m = g (mod 4): the F
+    // stage m % SF holds both tiles, A stage g (64 columns) receives them.
+    // Warp q of the group converts rows 32q.. into TMEM lanes 32q.. (the
+    // lane quarter its warp may write).
     const int grp = (warp - kWarpDq0) >> 2;
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol;
-    // Step n sits in F stage n / 2 at tile offset (n % 2) * tile_bytes.
-    int sf = grp >> 1, sa = grp;      // ring stages of this group's next step
-    const uint32_t f_off = static_cast<uint32_t>(grp & 1) * static_cast<uint32_t>(a.tile_bytes);
+    const uint32_t t_st = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
+                          static_cast<uint32_t>(grp) * 64u;
+    int sf = grp;
     uint32_t phf = 0, pha = 0;
     uint32_t n = 0;                   // K steps of this CTA before the unit
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      for (int ks = (grp - static_cast<int>(n)) & 3; ks < a.ksteps; ks += 4) {
+      for (int ks = 2 * ((grp - static_cast<int>(n >> 1)) & 3); ks < a.ksteps; ks += 8) {
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        const uint8_t* f = smem + C::kFOff + sf * C::kFStage + f_off;
-        const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
-        const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
-        uint32_t s0, s1, s2, s3;      // bf16 scale pairs of the 16-wide groups
-        if (a.gran == 16) {
-          const uint8_t* sc = f + kTileDataBytes + r * 4;
-          s0 = sc[0] * smul2 + sadd2;
-          s1 = sc[1] * smul2 + sadd2;
-          s2 = sc[2] * smul2 + sadd2;
-          s3 = sc[3] * smul2 + sadd2;
-        } else {
-          const uint8_t* sc = f + kTileDataBytes + r * 2;
-          s0 = s1 = sc[0] * smul2 + sadd2;
-          s2 = s3 = sc[1] * smul2 + sadd2;
-        }
-        // The A stage must be free before the first TMEM store; the F stage
-        // is released once both K halves have been converted.
-        if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
+        if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
         tc_fence_after();             // after the MMA that last read this stage
-        const uint32_t t_st = t_row + sa * 32u;
-        {
-          const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
-          const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
-          const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                  w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-          tmem_st16(t_st, v);
-        }
-        {
-          const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
-          const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
-          const uint32_t v[16] = {w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
-                                  w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
-          tmem_st16(t_st + 16u, v);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint8_t* f = smem + C::kFOff + sf * C::kFStage + t * a.tile_bytes;
+          const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
+          const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
+          uint32_t s0, s1, s2, s3;    // bf16 scale pairs of the 16-wide groups
+          if (a.gran == 16) {
+            const uint8_t* sc = f + kTileDataBytes + r * 4;
+            s0 = sc[0] * smul2 + sadd2;
+            s1 = sc[1] * smul2 + sadd2;
+            s2 = sc[2] * smul2 + sadd2;
+            s3 = sc[3] * smul2 + sadd2;
+          } else {
+            const uint8_t* sc = f + kTileDataBytes + r * 2;
+            s0 = s1 = sc[0] * smul2 + sadd2;
+            s2 = s3 = sc[1] * smul2 + sadd2;
+          }
+          {
+            const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
+            const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
+            const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                    w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+            tmem_st16(t_st + t * 32u, v);
+          }
+          {
+            const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
+            const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
+            const uint32_t v[16] = {w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
+                                    w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
+            tmem_st16(t_st + t * 32u + 16u, v);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(emptyF(sf));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aready(sa));
-        sf += 2;
+        if (lane == 0) mbar_arrive(aready(grp));
+        sf += 4;
         if (sf >= SF) { sf -= SF; phf ^= 1u; }
-        sa += 4;
-        if (sa >= SAa) { sa -= SAa; pha ^= 1u; }
+        pha ^= 1u;
       }
       n += static_cast<uint32_t>(a.ksteps);
     }
@@ -572,8 +589,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         // Sum the partial accumulators (NT columns apart) of the MMA warps
         // that had K steps in this unit: warp m took the steps with
         // (n_unit + ks) % kMmaWarps == m, none when ksteps is short.
-        const int m0 = static_cast<int>(n_unit % C::kMmaWarps);
-        const int nparts = min(C::kMmaWarps, a.ksteps);
+        const int m0 = static_cast<int>((n_unit >> 1) % C::kMmaWarps);
+        const int nparts = min(C::kMmaWarps, a.ksteps / 2);
         for (int j = part; live && j < nchunks; j += kParts) {
           uint32_t v[16];
           tmem_ld16(t_base + static_cast<uint32_t>(m0 * NT) + 16 * j, v);
