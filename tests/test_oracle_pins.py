@@ -393,26 +393,30 @@ def test_moe_one_expert_top1_is_dense_gemm(orc, w13_layout):
                                    atol=1e-12 * np.abs(ref).max())
 
 
-def test_moe_fp8_one_expert_top1_is_dense_gemm(orc):
+@pytest.mark.parametrize("gran", [32, 16])
+def test_moe_fp8_one_expert_top1_is_dense_gemm(orc, gran):
     E, K, I, T = 1, 64, 96, 4
     w = _tiny_weights(E, K, I, 42)
-    # group32 UE8M0 weights, as the FP8 path consumes them after requant
-    w13 = w["w13"].reshape(-1, K // 2)
-    w13q, w13s = orc.requant(w13, w["w13_s"].reshape(-1, K // 16))
-    w2q, w2s = orc.requant(w["w2"].reshape(-1, I // 2),
-                           w["w2_s"].reshape(-1, I // 16))
-    w32 = dict(w13=w13q.reshape(w["w13"].shape),
-               w13_s=w13s.reshape(E, 2 * I, K // 32), w13_gs=w["w13_gs"],
-               w2=w2q.reshape(w["w2"].shape), w2_s=w2s.reshape(E, K, I // 32),
-               w2_gs=w["w2_gs"])
+    if gran == 32:
+        # group32 UE8M0 weights, as the FP8 path consumes them after requant
+        w13 = w["w13"].reshape(-1, K // 2)
+        w13q, w13s = orc.requant(w13, w["w13_s"].reshape(-1, K // 16))
+        w2q, w2s = orc.requant(w["w2"].reshape(-1, I // 2),
+                               w["w2_s"].reshape(-1, I // 16))
+        wg = dict(w13=w13q.reshape(w["w13"].shape),
+                  w13_s=w13s.reshape(E, 2 * I, K // 32), w13_gs=w["w13_gs"],
+                  w2=w2q.reshape(w["w2"].shape), w2_s=w2s.reshape(E, K, I // 32),
+                  w2_gs=w["w2_gs"])
+    else:
+        wg = w   # group16 weights kept under FP8 activations
     g = np.random.default_rng(10)
     xb = synth.f32_to_bf16_bits(g.standard_normal((T, K)).astype(np.float32))
     xq, xs = orc.act_quant(xb)
     logits = g.standard_normal((T, E)).astype(np.float32)
-    y = orc.moe_rows(range(T), **w32, gran=32, w13_layout=0, act_mode=1,
+    y = orc.moe_rows(range(T), **wg, gran=gran, w13_layout=0, act_mode=1,
                      top_k=1, logits=logits, xq=xq, xs=xs)
-    W13 = _dequant(w32["w13"], w32["w13_s"], 32, w["w13_gs"])[0]
-    W2 = _dequant(w32["w2"], w32["w2_s"], 32, w["w2_gs"])[0]
+    W13 = _dequant(wg["w13"], wg["w13_s"], gran, w["w13_gs"])[0]
+    W2 = _dequant(wg["w2"], wg["w2_s"], gran, w["w2_gs"])[0]
     xv = torch_e4m3(xq) * np.repeat(torch_ue8m0(xs), 32, axis=1)
     for t in range(T):
         ref = _dense_reference(xv[t], W13, W2, 0, 1, I)
