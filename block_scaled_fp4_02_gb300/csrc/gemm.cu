@@ -64,8 +64,8 @@ struct Cfg {
   // One thread issues a tcgen05.mma about every 55 cycles whatever its size,
   // while the tensor pipe takes a short (N <= 32, A in TMEM) one every ~14:
   // with A in TMEM four warps issue, one per SM sub-partition (warp % 4),
-  // and split the K steps; with A in shared memory two MMA warps each own
-  // one weight tile (all K steps).
+  // and split the pairs of K steps; with A in shared memory two MMA warps
+  // each own one weight tile (all K steps).
   static constexpr int kMmaWarps = kATmem ? 4 : 2;
   static constexpr int kEpiWarps = kATmem ? 4 : 8;
   // The warps after the epilogue: TMEM A, the four MMA warps and then two
@@ -77,7 +77,8 @@ struct Cfg {
   static constexpr int kWarps = kATmem ? kWarpBX0 + kExtraB : kWarpMmaX0 + 1;
   static constexpr int kThreads = kWarps * 32;
   // Rings: F (packed weights, from HBM), A (dequantized weights, shared
-  // memory or TMEM), B (activation rows, from L2 by TMA).
+  // memory or TMEM), B (activation rows, from L2 by TMA).  With A in TMEM
+  // an F stage and an A stage hold a pair of K steps, a B stage one step.
   static constexpr int kStepsPerF = kATmem ? 2 : 1;  // K steps per F stage
   static constexpr int kSF = kATmem ? 12 : 6;
   static constexpr int kSAa = kATmem ? 4 : 2;      // TMEM A: 4 x 64 columns (two K tiles)
@@ -92,10 +93,9 @@ struct Cfg {
   static constexpr int kAccBufs = kATmem ? 2 : 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
   // Dequant warps per stage: TMEM A splits the 16 warps into four groups of
-  // four (one row quarter and the whole 64-wide K step each), NT=256 into
+  // four (one row quarter and a whole pair of K steps each), NT=256 into
   // two groups of eight (row quarter x K half) that fill one tile each.
   static constexpr int kDqPerStage = kATmem ? 4 : kDqGroups * kDqWarps;
-  // F stages are released by both groups whose steps they hold.
   static constexpr int kDqPerF = kATmem ? 4 : kDqGroups * kDqWarps;
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = kAOff + kAStage * kSAa;
@@ -111,7 +111,7 @@ struct Cfg {
                           kATmemCol + 64 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
   static_assert(!kATmem || (kSB == 2 * kSAa && kSF % 4 == 0 && kSAa == 4),
-                "TMEM A rings: shared A/B release, four dequant groups");
+                "TMEM A rings: B stages released with their pair's A stage");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
 };
