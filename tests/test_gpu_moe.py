@@ -332,3 +332,19 @@ def test_moe_full_size_fp8_keep_group16(orc):
     check_moe(orc, fp4, cfg, p, y, ws, toks, ref_y, ref_h, aux, w, 16, 1,
               acts["logits"], "fp8 keep group16, full size")
     p.free()
+
+
+@pytest.mark.parametrize("E,K,I,T,k", [
+    (1, 128, 128, 40, 1),     # smallest shapes: one K step pair, one expert
+    (16, 256, 128, 50, 16),   # top_k = E = 16 (every expert, largest k)
+    (3, 384, 256, 700, 3),    # many tokens, odd expert count, k = E
+    (5, 128, 384, 90, 2),     # T in (64, 256]: 256-token chunks, few per expert
+])
+def test_moe_edge_shapes(orc, E, K, I, T, k):
+    cfg = synth.MoeConfig(f"edge_E{E}_K{K}_I{I}_T{T}_k{k}", E, K, I, T, k,
+                          weight_seed=5000 + E + K + I, input_seed=6000 + T)
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w)
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=cfg.name)
