@@ -46,6 +46,16 @@ WORKLOADS = {"prefill": synth.PREFILL, "decode": synth.DECODE,
                  4096, 8, act="fp8", weight_seed=1005, input_seed=2005,
                  keep_group16=True),
              "tiny": synth.TINY,
+             # small-M decode on the decode weights (T = 1, 4, 16 tokens)
+             "decode_t1": synth.MoeConfig(
+                 "decode_w4a16_E256_K6144_I2048_T1_k8", 256, 6144, 2048, 1, 8,
+                 weight_seed=1003, input_seed=2101),
+             "decode_t4": synth.MoeConfig(
+                 "decode_w4a16_E256_K6144_I2048_T4_k8", 256, 6144, 2048, 4, 8,
+                 weight_seed=1003, input_seed=2104),
+             "decode_t16": synth.MoeConfig(
+                 "decode_w4a16_E256_K6144_I2048_T16_k8", 256, 6144, 2048, 16,
+                 8, weight_seed=1003, input_seed=2116),
              # small cases of the same kernels for ncu captures (inputs larger
              # than L2, a few GB on the device at most)
              "prefill_small": synth.MoeConfig(
@@ -66,7 +76,8 @@ def parse_args():
     ap.add_argument("--impl", default="fp4moe",
                     choices=["fp4moe", "reference"])
     ap.add_argument("--workload", default="prefill", choices=sorted(WORKLOADS))
-    ap.add_argument("--extra", default="decode,decode_skew,fp8,fp8_g16,requant",
+    ap.add_argument("--extra", default="decode,decode_skew,decode_t1,decode_t4,"
+                    "decode_t16,fp8,fp8_g16,requant",
                     help="comma list of extra workloads, or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -278,6 +289,14 @@ class MoeRun:
         return (self.touched * self.w13_bytes_per_expert + P * c.K * 2 +
                 P * c.I * (4 if self.fp8 else 2))
 
+    def fc2_bytes(self) -> int:
+        """Algorithmic FC2 bytes: touched experts' packed FC2 weights, h read
+        once and the FP32 FC2 output written once."""
+        c = self.cfg
+        P = c.T * c.top_k
+        return (self.touched * self.w2_bytes_per_expert + P * c.I * 2 +
+                P * c.K * 4)
+
     def free(self):
         self.packed.free()
 
@@ -304,37 +323,61 @@ def measured_traffic(workload: str):
         return None
 
 
-def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src, long_step):
+def tensor_peak(pk, fp8: bool):
+    """Dense tensor peak for the workload's arithmetic: the measured bf16
+    burst (a step of a few ms is timed, not a seconds-long loop); for the
+    FP8 x FP4 workload, whose roofline is the FP8 dense rate, twice that (the
+    nominal FP8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    bf16 = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return (2.0 * bf16 if fp8 else bf16), bf16
+
+
+def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src):
     cfg = run.cfg
     s = total_ms / 1e3
     tok = cfg.T * steps / s
     tflops = cfg.flops * steps / s / 1e12
     wgbs = run.weight_bytes() * steps / s / 1e9
-    fc1_ms = stages["fc1_swiglu"]
-    fc1_flops = 4 * cfg.K * cfg.I * cfg.T * cfg.top_k
+    fc1_ms, fc2_ms = stages["fc1_swiglu"], stages["fc2"]
+    P = cfg.T * cfg.top_k
+    fc1_flops = 4 * cfg.K * cfg.I * P
+    fc2_flops = 2 * cfg.K * cfg.I * P
+    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     out = {"tokens_per_s": tok, "ms_per_step": total_ms / steps,
            "tflops": tflops, "weight_gbs": wgbs,
            "touched_experts": run.touched, "stage_ms": stages}
-    tensor_bound = cfg.T * cfg.top_k / cfg.E >= 64
-    peak_key = "bf16_tflops_sustained" if long_step else "bf16_tflops"
+    tensor_bound = P / cfg.E >= 64
+    peak, bf16 = tensor_peak(pk, run.fp8)
+    pname = ("2 x measured bf16_tflops (FP8 dense)" if run.fp8 else
+             "bf16_tflops (burst)")
     if tensor_bound:
         ach = fc1_flops / (fc1_ms / 1e3) / 1e12
-        peak = float(pk.get(peak_key, FALLBACK_PEAKS[peak_key]))
         roof = {"bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
-                "peak_source": f"{pk_src} {peak_key}",
+                "peak_source": f"{pk_src} {pname}",
                 "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
                 "per_launch_flops": fc1_flops,
                 "per_launch_bytes": run.fc1_bytes()}
+        fc2 = fc2_flops / (fc2_ms / 1e3) / 1e12
+        out["fc2_roofline"] = {"bound": "tensor", "achieved": fc2,
+                               "peak": peak, "unit": "TFLOP/s",
+                               "frac": fc2 / peak}
+        out["layer_tensor_frac"] = tflops / peak
+        if run.fp8:
+            out["frac_vs_bf16_peak"] = {"fc1": ach / bf16, "fc2": fc2 / bf16,
+                                        "layer": tflops / bf16}
     else:
         ach = run.fc1_bytes() / (fc1_ms / 1e3) / 1e9
-        peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "peak_source": f"{pk_src} hbm_gbs",
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": f"{pk_src} hbm_gbs",
                 "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
                 "per_launch_bytes": run.fc1_bytes()}
+        fc2 = run.fc2_bytes() / (fc2_ms / 1e3) / 1e9
+        out["fc2_roofline"] = {"bound": "hbm", "achieved": fc2, "peak": hbm,
+                               "unit": "GB/s", "frac": fc2 / hbm,
+                               "per_launch_bytes": run.fc2_bytes()}
     roof["traffic"] = measured_traffic(cfg.name)
-    out["layer_hbm_frac"] = wgbs / float(pk.get("hbm_gbs", 6800.0))
+    out["layer_hbm_frac"] = wgbs / hbm
     return out, roof
 
 
@@ -470,8 +513,7 @@ def main():
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    head, roof = summarize(run, total_ms, stages, args.steps, pk, pk_src,
-                           long_step=True)
+    head, roof = summarize(run, total_ms, stages, args.steps, pk, pk_src)
 
     e2e = None
     if not args.no_e2e:
@@ -514,7 +556,7 @@ def main():
         else:
             r = MoeRun(c, fp4, torch, synth.moe_weights(c))
         ms, st, _ = r.timed(args.steps, args.warmup)
-        sm, rf = summarize(r, ms, st, args.steps, pk, pk_src, long_step=False)
+        sm, rf = summarize(r, ms, st, args.steps, pk, pk_src)
         sm["roofline"] = rf
         sm["workload"] = c.name
         extra[name] = sm
@@ -543,6 +585,8 @@ def main():
                          f"{(run.packed.desc.w13_bytes + run.packed.desc.w2_bytes) / 1e9:.2f} GB)"},
         "tflops": head["tflops"] * world, "weight_gbs": head["weight_gbs"],
         "layer_hbm_frac": head["layer_hbm_frac"],
+        "layer_tensor_frac": head.get("layer_tensor_frac"),
+        "fc2_roofline": head["fc2_roofline"],
         "stage_ms": head["stage_ms"], "touched_experts": run.touched,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": run.launches_per_step * args.steps,

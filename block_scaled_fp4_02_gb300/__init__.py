@@ -24,6 +24,7 @@ __all__ = [
     "prepare_weights", "PackedWeights", "moe_workspace_size", "moe_forward",
     "moe_workspace_size_host", "moe_forward_host", "status_string",
     "last_device_error", "set_stage_events", "STAGE_NAMES",
+    "test_wait_timeout",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, \
@@ -106,6 +107,7 @@ def load() -> ctypes.CDLL:
             "fp4moe_set_stage_events": (i32, [ctypes.POINTER(vp), i32]),
             "fp4moe_moe_workspace_offsets": (i32, [vp, i32, i32,
                                                    ctypes.POINTER(sz), i32]),
+            "fp4moe_test_wait_timeout": (i32, [ctypes.c_uint64, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -169,6 +171,14 @@ def set_stage_events(events) -> None:
 def last_device_error() -> int:
     """Reads and clears the device status word (synchronises)."""
     return load().fp4moe_last_device_error()
+
+
+def test_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launches the bounded-wait self-test: a wait on an mbarrier that nothing
+    completes gives up after limit_ns and records ERR_TIMEOUT in the device
+    status word (read it with last_device_error())."""
+    _check(load().fp4moe_test_wait_timeout(limit_ns, _stream(stream)),
+           "test_wait_timeout")
 
 
 # ------------------------------------------------------------------- steps

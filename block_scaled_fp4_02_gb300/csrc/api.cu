@@ -29,6 +29,20 @@ int* status_word() {
   if (cudaGetSymbolAddress(&p, g_fp4moe_status) != cudaSuccess) return nullptr;
   return static_cast<int*>(p);
 }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
 }  // namespace fp4moe
 
 namespace {
@@ -37,20 +51,6 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
-
-int sm_count() {
-  static std::mutex mu;
-  static int cache[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> g(mu);
-  if (dev < 64 && cache[dev] == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 1;
-  }
-  return dev < 64 ? cache[dev] : 1;
-}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -417,7 +417,7 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   int* err = status_word();
   const int64_t P = static_cast<int64_t>(T) * top_k;
   const int chunk = gemm_chunk_max(T);
-  const int sms = sm_count();
+  const int sms = device_sm_count();
 
   struct StageOff {  // the hand-over covers exactly one forward call
     ~StageOff() { t_stage_on = false; }

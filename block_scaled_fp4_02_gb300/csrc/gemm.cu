@@ -41,11 +41,15 @@
 //                 n = 2, 3 (mod 4).
 // All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
 // the device status word and the CTA winds down and frees its TMEM.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace fp4moe {
 namespace {
+
+constexpr int kMaxDevices = 64;
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kDqGroups = 2;     // dequant groups (A in shared memory)
@@ -626,16 +630,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   }
 }
 
+// The dynamic shared-memory opt-in is a per-device function attribute: it is
+// set once per device (and kernel instantiation), under a lock.
 template <int NT, int MODE>
 cudaError_t launch_one(const CUtensorMap& tmB, const GemmArgs& a, int grid,
                        cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<NT, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg<NT>::kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+  static std::mutex mu;
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(moe_gemm_kernel<NT, MODE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Cfg<NT>::kSmem));
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
   }
   moe_gemm_kernel<NT, MODE><<<grid, Cfg<NT>::kThreads, Cfg<NT>::kSmem, st>>>(tmB, a);
   return cudaGetLastError();

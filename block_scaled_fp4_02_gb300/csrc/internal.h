@@ -98,4 +98,12 @@ int gemm_box_rows(int chunk);
 // Device address of the per-device status word (kernels record errors there).
 int* status_word();
 
+// Number of SMs of the current device (cached per device, thread-safe).
+int device_sm_count();
+
+// Test helper: one thread waits, with a bounded wait of limit_ns, on an
+// mbarrier that nothing completes, and records TIMEOUT in *err.
+cudaError_t launch_wait_timeout(unsigned long long limit_ns, int* err,
+                                cudaStream_t st);
+
 }  // namespace fp4moe

@@ -12,16 +12,7 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 1;
-  }
-  return g_num_sms;
-}
+int num_sms() { return device_sm_count(); }
 
 // ================================================================ requant
 //

@@ -32,7 +32,10 @@
 extern "C" {
 #endif
 
-/* Status codes. */
+/* Status codes.  INVALID_ARG mirrors the prepare page's validation errors
+ * (shape, dtype, divisibility); UNSUPPORTED mirrors the capability gate of
+ * the group16 notes page (section "Current patch scope": a recipe the fused
+ * compute refuses); TIMEOUT and CUDA_ERROR have no counterpart there. */
 enum fp4moe_status {
   FP4MOE_OK = 0,
   FP4MOE_ERR_INVALID_ARG = 1,         /* bad shape, pointer, enum or value  */
@@ -147,8 +150,23 @@ void fp4moe_free_packed(fp4moe_packed* p);
 int fp4moe_packed_info(const fp4moe_packed* p, fp4moe_packed_desc* desc);
 
 /* -------------------------------------------------------------- S2..S7 --
- * Bytes of device workspace moe_forward needs for T tokens and top_k.
- * Returns 0 for invalid arguments. */
+ * Sources of the MoE layer.  The pages print no kernel for routing,
+ * permutation, SwiGLU or combine; these calls follow the benchmark
+ * description of the MoE workloads (the tiny layer E8 K256 I128 T16 top-2,
+ * the decode layer E256 K6144 I2048 T64 top-8, the prefill layer T8192, the
+ * FP8 x FP4 layer E128 K7168 I2048 T4096 top-8): router logits FP32, softmax
+ * then top-k with the k weights renormalised, SwiGLU(gate, up), FP32
+ * accumulation, bfloat16 output; the expert FFN is routing -> top-k
+ * permutation (per-expert histogram, prefix-sum offsets, scatter) -> FC1
+ * gate|up grouped GEMM with SwiGLU -> FC2 grouped GEMM -> weighted top-k
+ * combine.  The gate/up row order is the prepare page's (W13 layout notes);
+ * the FP8 activation format is recipe (1,1,32) of the group16 notes page
+ * (section "Context").
+ *
+ * Bytes of device workspace moe_forward needs for T tokens and top_k: the
+ * routing scratch, ids and weights, counts and offsets, perm and inv, the
+ * gathered activation rows, h and the FC2 output (FP32), laid out for the
+ * steps above.  Returns 0 for invalid arguments. */
 size_t fp4moe_moe_workspace_size(const fp4moe_packed* p, int T, int top_k);
 
 /* MoE layer forward: softmax top-k routing with renormalised weights (S2),
@@ -169,7 +187,8 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
                        const fp4moe_packed* p, int top_k, void* y,
                        void* workspace, size_t ws_bytes, void* stream);
 
-/* End-to-end variant for callers holding HOST buffers: x_host, x_scales_host
+/* End-to-end variant of moe_forward (same steps and sources as above) for
+ * callers holding HOST buffers: x_host, x_scales_host
  * (FP8 mode) and logits_host are copied to the device, moe_forward runs, and
  * y is copied back to y_host, all asynchronously on `stream` (use pinned host
  * memory; synchronise the stream before reading y_host).  The device
@@ -181,7 +200,9 @@ int fp4moe_moe_forward_host(const void* x_host, const uint8_t* x_scales_host,
                             const fp4moe_packed* p, int top_k, void* y_host,
                             void* workspace, size_t ws_bytes, void* stream);
 
-/* Test export: byte offsets, inside the moe_forward workspace for (p, T,
+/* Test export (no counterpart on the pages; it exposes moe_forward's own
+ * intermediates so tests can check each step): byte offsets, inside the
+ * moe_forward workspace for (p, T,
  * top_k), of its intermediates, so a test can read them back after a call:
  * out[0] ids int32 [T*top_k], [1] routing weights FP32 [T*top_k], [2] counts
  * int32 [E], [3] offsets int32 [E+1], [4] perm int32 [P], [5] inv int32 [P],
@@ -191,7 +212,10 @@ int fp4moe_moe_forward_host(const void* x_host, const uint8_t* x_scales_host,
 int fp4moe_moe_workspace_offsets(const fp4moe_packed* p, int T, int top_k,
                                  size_t* out, int n);
 
-/* Test export of S2 + S3 alone (bit-exact checks): ids [T, top_k] int32,
+/* Test export of S2 + S3 alone (bit-exact checks), defined by the routing of
+ * the benchmark description's MoE workloads (softmax then top-k with
+ * renormalised weights) and its top-k permutation (per-expert histogram,
+ * prefix-sum offsets, scatter): ids [T, top_k] int32,
  * w [T, top_k] FP32, counts [E], offsets [E+1], perm [T*top_k],
  * inv [T*top_k], with workspace >= fp4moe_route_workspace_size(T, E, top_k).
  * Ties between equal logits go to the lower expert id; pairs p = t*top_k + j
@@ -230,6 +254,9 @@ int fp4moe_set_stage_events(void* const* events, int n);
  *   - All calls share the one array, and each call overwrites what it uses,
  *     so calls whose kernels overlap on the GPU (other streams, other host
  *     threads) race on it: serialise them.
+ *   - The looked-up address belongs to the device's current context: after
+ *     cudaDeviceReset (or anything else that destroys that context) it is
+ *     stale, so do not call this entry point across a device reset.
  *   - Sizes whose scratch (fp4moe_route_noalloc_scratch_bytes) exceeds the
  *     array return FP4MOE_ERR_WORKSPACE_TOO_SMALL before launching anything;
  *     the scratch is about 8 * ceil(T/32) * E bytes, so 4 MiB covers, e.g.,
@@ -241,10 +268,20 @@ int fp4moe_route_noalloc(const float* logits, int T, int E, int top_k,
                          int32_t* offsets, int32_t* perm, int32_t* inv,
                          void* stream);
 
-/* Static text for a status code (never NULL). */
+/* Test export of the bounded device waits (no counterpart on the pages):
+ * launches one thread that waits on an mbarrier nothing completes; the wait
+ * gives up after limit_ns nanoseconds (1 .. 1e9, else INVALID_ARG) and records
+ * FP4MOE_ERR_TIMEOUT in the device status word, which
+ * fp4moe_last_device_error() then returns.  Every wait inside the library's
+ * kernels is bounded the same way (about 2 s).  Asynchronous on `stream`. */
+int fp4moe_test_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Static text for a status code (never NULL); see the status codes above. */
 const char* fp4moe_status_string(int status);
 
-/* Reads and clears the status word of the current device: the first error a
+/* Device-side error reporting (no counterpart on the pages, whose code only
+ * raises host exceptions): reads and clears the status word of the current
+ * device: the first error a
  * kernel recorded since the last call (FP4MOE_OK if none).  Synchronises the
  * device.  Returns FP4MOE_ERR_CUDA if the read itself fails. */
 int fp4moe_last_device_error(void);

@@ -102,3 +102,11 @@ def test_moe_argument_checks(lib):
     assert lib.fp4moe_moe_forward_host(FAKE, None, FAKE, 8, None, 2, FAKE,
                                        FAKE, 1 << 20, None) == \
         fp4.ERR_INVALID_ARG
+
+
+def test_wait_timeout_argument_checks(lib):
+    f = lib.fp4moe_test_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    assert f(0, None) == fp4.ERR_INVALID_ARG
+    assert f(2_000_000_000, None) == fp4.ERR_INVALID_ARG

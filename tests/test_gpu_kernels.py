@@ -191,3 +191,21 @@ def test_route_nan_logit_is_reported():
     logits[2, 3] = float("nan")
     fp4.route_debug(logits, 2)
     assert fp4.last_device_error() == fp4.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------- bounded device waits
+
+def test_bounded_wait_gives_up_and_records_timeout():
+    # A wait on an mbarrier that nothing completes gives up after its limit
+    # (1 ms here; the library's kernels use about 2 s) and records TIMEOUT in
+    # the status word; the context stays usable afterwards.
+    assert fp4.last_device_error() == fp4.OK
+    fp4.test_wait_timeout(1_000_000)
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == fp4.ERR_TIMEOUT
+    assert fp4.last_device_error() == fp4.OK      # read clears it
+    x = torch.arange(64, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 2016.0
+    codes, scales, _ = synth.requant_inputs(synth.SMALL_REQUANT)
+    gpu_requant(codes, scales)
+    assert fp4.last_device_error() == fp4.OK

@@ -63,7 +63,7 @@ def gpu_forward(p, acts, k, act):
 
 
 def check_against_oracle(orc, cfg, w, acts, p, y, ws, tokens, layout=0,
-                         gran=16, what=None):
+                         gran=16, what=None, record=None):
     """Oracle rows for `tokens`, then the two-level (h, y) parity check."""
     tokens = list(tokens)
     if cfg.act == "fp8":
@@ -81,7 +81,8 @@ def check_against_oracle(orc, cfg, w, acts, p, y, ws, tokens, layout=0,
                                     top_k=cfg.top_k, logits=acts["logits"],
                                     x_bf16=acts["x_bf16"], return_h=True)
     return check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, aux,
-                     w_used, gran, act, acts["logits"], what or cfg.name)
+                     w_used, gran, act, acts["logits"], what or cfg.name,
+                     record=record)
 
 
 # ------------------------------------------------------------------ layout
@@ -132,7 +133,7 @@ SMALL = [synth.TINY, synth.SMALL_DECODE, synth.SMALL_PREFILL, synth.SMALL_FP8]
 
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
 @pytest.mark.parametrize("layout", [0, 1])
-def test_moe_small_configs_all_tokens(orc, cfg, layout):
+def test_moe_small_configs_all_tokens(orc, cfg, layout, record_property):
     w = weights_for(cfg)
     if layout == 1:
         w = swap_halves(w, cfg.I)
@@ -141,10 +142,11 @@ def test_moe_small_configs_all_tokens(orc, cfg, layout):
     p = prepare(w, layout=layout, act=act)
     y, ws = gpu_forward(p, acts, cfg.top_k, act)
     check_against_oracle(orc, cfg, w, acts, p, y, ws, range(cfg.T),
-                         layout=layout)
+                         layout=layout,
+                         record=record_property)
 
 
-def test_moe_group32_weights_bf16_activations(orc):
+def test_moe_group32_weights_bf16_activations(orc, record_property):
     # W4A16 over MX (UE8M0 group32) weights, no requant on the GPU side.
     cfg = synth.SMALL_DECODE
     w32 = requant_weights_oracle(orc, weights_for(cfg), cfg.E, cfg.K, cfg.I)
@@ -152,7 +154,8 @@ def test_moe_group32_weights_bf16_activations(orc):
     p = prepare(w32, gran=32)
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
     check_against_oracle(orc, cfg, w32, acts, p, y, ws, range(cfg.T), gran=32,
-                         what="group32 bf16")
+                         what="group32 bf16",
+                         record=record_property)
 
 
 def _fp8_group16_oracle(orc, cfg, w, acts, tokens):
@@ -162,7 +165,7 @@ def _fp8_group16_oracle(orc, cfg, w, acts, tokens):
                         return_h=True)
 
 
-def test_moe_fp8_keep_group16(orc):
+def test_moe_fp8_keep_group16(orc, record_property):
     # FP8 activations over group16 weights without the lossy requant: the
     # oracle runs the group16 weights as they are.
     cfg = synth.SMALL_FP8
@@ -174,7 +177,7 @@ def test_moe_fp8_keep_group16(orc):
     tokens = list(range(cfg.T))
     ref_y, ref_h, aux = _fp8_group16_oracle(orc, cfg, w, acts, tokens)
     check_moe(orc, fp4, cfg, p, y, ws, tokens, ref_y, ref_h, aux, w, 16, 1,
-              acts["logits"], "fp8 keep group16")
+              acts["logits"], "fp8 keep group16", record=record_property)
 
 
 def test_fp8_group16_accuracy_gap(orc, record_property):
@@ -224,7 +227,7 @@ def test_moe_inverted_global_scales():
 
 
 @pytest.mark.parametrize("T", [1, 2, 17, 300])
-def test_moe_token_counts(orc, T):
+def test_moe_token_counts(orc, T, record_property):
     base = synth.SMALL_DECODE
     cfg = synth.MoeConfig("t", base.E, base.K, base.I, T, base.top_k,
                           weight_seed=base.weight_seed, input_seed=900 + T)
@@ -232,11 +235,12 @@ def test_moe_token_counts(orc, T):
     acts = synth.moe_activations(cfg)
     p = prepare(w)
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
-    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=f"T={T}")
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=f"T={T}",
+                         record=record_property)
 
 
 @pytest.mark.parametrize("k", [1, 2])
-def test_moe_hot_experts_get_every_token(orc, k):
+def test_moe_hot_experts_get_every_token(orc, k, record_property):
     # The first k experts win every token: 600 tokens per expert, so each
     # expert is split into several token chunks.
     cfg = synth.MoeConfig("hot", 8, 768, 384, 600, k, weight_seed=3002,
@@ -248,7 +252,8 @@ def test_moe_hot_experts_get_every_token(orc, k):
     p = prepare(w)
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
     check_against_oracle(orc, cfg, w, acts, p, y, ws, range(cfg.T),
-                         what=f"hot experts k={k}")
+                         what=f"hot experts k={k}",
+                         record=record_property)
 
 
 def test_moe_zero_tokens_is_noop():
@@ -306,7 +311,7 @@ def _sample_tokens(T, n, seed):
 @pytest.mark.parametrize("cfg,n", [(synth.DECODE, 64), (synth.DECODE_SKEW, 64),
                                    (synth.PREFILL, 24), (synth.FP8, 24)],
                          ids=lambda c: getattr(c, "name", str(c)))
-def test_moe_full_size_sampled(orc, cfg, n):
+def test_moe_full_size_sampled(orc, cfg, n, record_property):
     """Full-size workloads in the benchmark's launch configuration; the
     oracle recomputes a sample of output rows one token at a time."""
     w = weights_for(cfg)
@@ -315,11 +320,12 @@ def test_moe_full_size_sampled(orc, cfg, n):
     p = prepare(w, act=act)
     y, ws = gpu_forward(p, acts, cfg.top_k, act)
     toks = _sample_tokens(cfg.T, n, 99)
-    check_against_oracle(orc, cfg, w, acts, p, y, ws, toks)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, toks,
+                         record=record_property)
     p.free()
 
 
-def test_moe_full_size_fp8_keep_group16(orc):
+def test_moe_full_size_fp8_keep_group16(orc, record_property):
     """The FP8 workload with its group16 weights kept (no requant), sampled
     rows against the oracle over the group16 weights."""
     cfg = synth.FP8
@@ -330,7 +336,8 @@ def test_moe_full_size_fp8_keep_group16(orc):
     toks = _sample_tokens(cfg.T, 24, 98)
     ref_y, ref_h, aux = _fp8_group16_oracle(orc, cfg, w, acts, toks)
     check_moe(orc, fp4, cfg, p, y, ws, toks, ref_y, ref_h, aux, w, 16, 1,
-              acts["logits"], "fp8 keep group16, full size")
+              acts["logits"], "fp8 keep group16, full size",
+              record=record_property)
     p.free()
 
 
@@ -340,11 +347,12 @@ def test_moe_full_size_fp8_keep_group16(orc):
     (3, 384, 256, 700, 3),    # many tokens, odd expert count, k = E
     (5, 128, 384, 90, 2),     # T in (64, 256]: 256-token chunks, few per expert
 ])
-def test_moe_edge_shapes(orc, E, K, I, T, k):
+def test_moe_edge_shapes(orc, E, K, I, T, k, record_property):
     cfg = synth.MoeConfig(f"edge_E{E}_K{K}_I{I}_T{T}_k{k}", E, K, I, T, k,
                           weight_seed=5000 + E + K + I, input_seed=6000 + T)
     w = weights_for(cfg)
     acts = synth.moe_activations(cfg)
     p = prepare(w)
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
-    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=cfg.name)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=cfg.name,
+                         record=record_property)
