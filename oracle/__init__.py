@@ -235,7 +235,9 @@ def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
     """MoE output rows y[t] in FP64 (before the final bf16 rounding), S2-S7.
 
     With return_h, also returns the unrounded intermediate h [ntok, k, I]
-    and aux [ntok, k, I, 4] = (G, U, sum|G terms|, sum|U terms|)."""
+    and aux [ntok, k, I, 6] = (G, U, sum|G terms|, sum|U terms|,
+    sum|G running sums|, sum|U running sums|), the running sums taken after
+    each chunk of 16 consecutive K terms (FP32 error-analysis quantities)."""
     E, twoI, kb = w13.shape
     K, I = kb * 2, twoI // 2
     T = logits.shape[0]
@@ -255,7 +257,7 @@ def moe_rows(tokens, *, w13, w13_s, w13_gs, w2, w2_s, w2_gs, gran,
         arrs["xs"] = np.ascontiguousarray(xs, dtype=np.uint8)
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
     h = np.empty((tok.size, top_k, I), dtype=np.float64) if return_h else None
-    aux = (np.empty((tok.size, top_k, I, 4), dtype=np.float64) if return_h
+    aux = (np.empty((tok.size, top_k, I, 6), dtype=np.float64) if return_h
            else None)
     args = _OrcMoe(
         _ptr(arrs["w13"]), _ptr(arrs["w13_s"]), _ptr(arrs["w13_gs"]),

@@ -325,7 +325,9 @@ int orc_act_quant(const uint16_t* x, int64_t T, int64_t K, uint8_t* q,
 //   y_t = sum_j w_{t,j} * o_{(t,j)}, in top-k order.  Returned in FP64; the
 //   product rounds y to bfloat16 (orc_bf16_rne gives that rounding).
 //   If h_out is set, the unrounded h of each (token, slot) is stored there;
-//   aux_out receives G, U and the sums of |terms| behind them.
+//   aux_out receives G, U, the sums of |terms| behind them and the sums of
+//   |running sums| after each 16-wide K chunk (error-analysis quantities for
+//   the tests' FP32 tolerance; they do not enter y).
 // act_mode 0 reads x_bf16 [T, K]; act_mode 1 reads xq [T, K] (E4M3) and
 // xs [T, K/32] (UE8M0).
 struct OrcMoe {
@@ -342,8 +344,10 @@ struct OrcMoe {
   const float* logits;
   int64_t T;
   double* h_out;  // optional [ntok, top_k, I]: h before its rounding
-  double* aux_out;  // optional [ntok, top_k, I, 4]: G, U, sum|G terms|,
-                    // sum|U terms| (the scale of FP32 rounding in G and U)
+  double* aux_out;  // optional [ntok, top_k, I, 6]: G, U, sum|G terms|,
+                    // sum|U terms|, sum over 16-wide K chunks of |G running
+                    // sum|, the same for U (the scale of FP32 rounding in G
+                    // and U); global scale included in all but G and U
 };
 
 static double weight_value(const uint8_t* w, const uint8_t* s, int gran,
@@ -356,16 +360,20 @@ static double weight_value(const uint8_t* w, const uint8_t* s, int gran,
 }
 
 // One row dot product: sum_k x[k] * dequant(w[row, k]) (FP64); *abs_sum
-// (if given) receives sum_k |x[k] * dequant(w[row, k])|.
+// (if given) receives sum_k |x[k] * dequant(w[row, k])| and *run_sum the sum,
+// over the chunks of 16 consecutive k, of |the running sum after the chunk|.
 static double row_dot(const uint8_t* w, const uint8_t* s, int gran, int64_t Kd,
-                      int64_t row, const double* x, double* abs_sum = nullptr) {
-  double acc = 0.0, a = 0.0;
+                      int64_t row, const double* x, double* abs_sum = nullptr,
+                      double* run_sum = nullptr) {
+  double acc = 0.0, a = 0.0, r = 0.0;
   for (int64_t k = 0; k < Kd; ++k) {
     const double t = x[k] * weight_value(w, s, gran, Kd, row, k);
     acc += t;
     a += std::fabs(t);
+    if (k % 16 == 15) r += std::fabs(acc);
   }
   if (abs_sum) *abs_sum = a;
+  if (run_sum) *run_sum = r;
   return acc;
 }
 
@@ -413,7 +421,8 @@ int orc_moe_rows(const OrcMoe* a, const int64_t* tokens, int64_t ntok,
   if (K % a->gran || I % a->gran) return 1;
   if (a->act_mode == 1 && (K % 32 || I % 32)) return 1;
   std::vector<int32_t> ids(a->top_k);
-  std::vector<double> w(a->top_k), x(K), g(I), u(I), h(I), o(K), sg(I), su(I);
+  std::vector<double> w(a->top_k), x(K), g(I), u(I), h(I), o(K), sg(I), su(I),
+      pg(I), pu(I);
   for (int64_t n = 0; n < ntok; ++n) {
     int64_t t = tokens[n];
     if (t < 0 || t >= a->T) return 1;
@@ -438,19 +447,23 @@ int orc_moe_rows(const OrcMoe* a, const int64_t* tokens, int64_t ntok,
       const int64_t up0 = (a->w13_layout == 0) ? I : 0;
       const double gs13 = a->w13_gs[e], gs2 = a->w2_gs[e];
       parallel_for(I, a->nthreads, [&](int64_t i) {
-        g[i] = gs13 * row_dot(w13, w13s, a->gran, K, gate0 + i, x.data(), &sg[i]);
-        u[i] = gs13 * row_dot(w13, w13s, a->gran, K, up0 + i, x.data(), &su[i]);
+        g[i] = gs13 * row_dot(w13, w13s, a->gran, K, gate0 + i, x.data(), &sg[i],
+                              &pg[i]);
+        u[i] = gs13 * row_dot(w13, w13s, a->gran, K, up0 + i, x.data(), &su[i],
+                              &pu[i]);
         h[i] = g[i] / (1.0 + std::exp(-g[i])) * u[i];
       });
       if (a->h_out)
         std::copy(h.begin(), h.end(), a->h_out + (n * a->top_k + j) * I);
       if (a->aux_out) {
-        double* ax = a->aux_out + (n * a->top_k + j) * I * 4;
+        double* ax = a->aux_out + (n * a->top_k + j) * I * 6;
         for (int64_t i = 0; i < I; ++i) {
-          ax[4 * i] = g[i];
-          ax[4 * i + 1] = u[i];
-          ax[4 * i + 2] = std::fabs(gs13) * sg[i];
-          ax[4 * i + 3] = std::fabs(gs13) * su[i];
+          ax[6 * i] = g[i];
+          ax[6 * i + 1] = u[i];
+          ax[6 * i + 2] = std::fabs(gs13) * sg[i];
+          ax[6 * i + 3] = std::fabs(gs13) * su[i];
+          ax[6 * i + 4] = std::fabs(gs13) * pg[i];
+          ax[6 * i + 5] = std::fabs(gs13) * pu[i];
         }
       }
       round_intermediate(h, a->act_mode);

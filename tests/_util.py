@@ -135,52 +135,62 @@ def dequant_reference(codes_packed, scales, gran, gs):
 # The intermediate h = silu(G) * U is rounded (bf16, or E4M3 x UE8M0/32)
 # between FC1 and FC2.  The GPU takes that decision from its FP32 value and
 # the oracle from its FP64 value, so where the exact h sits closer to a
-# rounding boundary than the FP32 error of G and U can reach, both codes are
-# correct roundings (several results are correct).  The check therefore
+# rounding boundary than the FP32 error of G and U can reach, more than one
+# code is a correct rounding (several results are correct).  The check
 #  (1) compares the GPU's h (read back from the workspace) with the oracle's
-#      rounded h.  They must be equal, except that the GPU's code may be the
-#      ADJACENT code (one bf16 ulp; in the FP8 path the neighbouring E4M3 code,
-#      or the rounding under the neighbouring group exponent when the group's
-#      maximum itself sits at an exponent boundary) when the exact h lies
-#      within the error radius r of the boundary between the two codes; and
-#      such elements may be at most MAX_TIE_FRAC of all h elements;
+#      rounded h.  They must be equal, except that the GPU's code may be a
+#      correct rounding of another value within the FP32 error radius r of
+#      the exact h: the adjacent code when h lies within r of the boundary
+#      between the two, and a code further away only where r itself spans
+#      more than one code (h near zero after cancellation in G or U); in the
+#      FP8 path also the rounding under the neighbouring group exponent when
+#      the group's maximum sits within its radius of an exponent boundary.
+#      Such ties may be at most MAX_TIE_FRAC of all h elements;
 #  (2) compares y with the oracle's y under the stated tolerance
 #      |d| <= 2^-7 |ref| + 1e-3 rms(ref), widened for an output element only
 #      by the exact effect of those tie choices, sum_j |w_j w2[c, i] dh_i|.
 #
-# The radius bounds the FP32 error of G and U with the probabilistic
-# accumulation bound lambda * sqrt(n) * u * sum|terms| (Higham and Mary,
-# "A new approach to probabilistic rounding error analysis", 2019), taken
-# with n = K additions, u = 2^-23 (so truncating accumulation is covered)
-# and lambda = 6 (failure probability below 2 exp(-18) per element), then
-# propagated through silu(G) * U to first order, plus 2^-17 |h| for the
-# epilogue's elementwise FP32 operations (fast exponential and division).
+# The radius is a first-order bound on the FP32 error of G (and U) under a
+# pessimistic model of the tensor core's accumulation: each K step adds 16
+# exact products to the running sum S, aligning the 17 addends to the
+# largest and truncating each (an error below u = 2^-23 of the largest,
+# <= 17 u max(|S_{s-1}|, max|t|) <= 17 u (|S_{s-1}| + sum_step |t|)), then
+# rounds the result (<= u |S_s|).  Summed over the steps:
+#     |G_fp32 - G| <= u (18 sum_s |S_s| + 17 sum_k |t_k|),
+# with S_s the running sums after each chunk of 16 and t_k the terms (the
+# oracle returns both sums in FP64).  The radius takes twice that (other
+# summation orders: partial accumulators summed in the epilogue, 32-wide
+# K steps), propagates it through silu(G) * U to first order and adds
+# 2^-17 |h| for the epilogue's elementwise FP32 operations (fast exponential
+# and division).
 #
 # MAX_TIE_FRAC: a tie can only occur where the exact h lies within the
 # GPU's error of a rounding boundary.  The bf16 boundaries are one ulp
 # apart (relative spacing 2^-8 .. 2^-7), so a relative error delta in h gives
 # a tie rate of about 2 delta / 2^-7.5 ~ 360 delta.  The highest rate seen on
-# the GB300 so far is 1.31e-3 (the decode workload: 1378 of 1,048,576 h
-# elements), i.e. delta ~ 3.6e-6 -- FP32 accumulation over 384 tensor-core
-# K steps plus the fast SiLU.  The cap allows 2.3x that rate (delta up to
-# ~8e-6); a systematic error of one ulp would flip half of all elements.
+# the GB300 is 1.31e-3 (the decode workload: 1378 of 1,048,576 h elements),
+# i.e. delta ~ 3.6e-6 -- FP32 accumulation over 384 tensor-core K steps plus
+# the fast SiLU.  The cap allows 2.3x that rate (delta up to ~8e-6); a
+# systematic error of one ulp would flip half of all elements.
 MAX_TIE_FRAC = 3e-3
-RADIUS_LAMBDA = 6.0
+RADIUS_MARGIN = 2.0
+U32 = 2.0 ** -23
 
 
 def _silu(g):
     return g / (1.0 + np.exp(-g))
 
 
-def moe_radius(aux, K):
-    """Error radius of the GPU's FP32 h, per element (aux from the oracle)."""
-    G, U, SG, SU = aux[..., 0], aux[..., 1], aux[..., 2], aux[..., 3]
-    gamma = RADIUS_LAMBDA * np.sqrt(K) * 2.0 ** -23
+def moe_radius(aux, K=None):
+    """FP32 error radius of the GPU's h, per element (aux from the oracle)."""
+    G, U = aux[..., 0], aux[..., 1]
+    SG, SU, PG, PU = aux[..., 2], aux[..., 3], aux[..., 4], aux[..., 5]
+    rG = RADIUS_MARGIN * U32 * (18.0 * PG + 17.0 * SG)
+    rU = RADIUS_MARGIN * U32 * (18.0 * PU + 17.0 * SU)
     sig = 1.0 / (1.0 + np.exp(-G))
     dsilu = sig * (1.0 + G * (1.0 - sig))
     h = _silu(G) * U
-    return (np.abs(U * dsilu) * gamma * SG + np.abs(_silu(G)) * gamma * SU
-            + 2.0 ** -17 * np.abs(h))
+    return np.abs(U * dsilu) * rG + np.abs(_silu(G)) * rU + 2.0 ** -17 * np.abs(h)
 
 
 def _bf16_bits(v) -> np.ndarray:
@@ -195,49 +205,58 @@ def _ordered(bits, sign_bit):
     return np.where(bits & sign_bit, -mag, mag)
 
 
-def _tie_bf16(h, r, vg, vo):
-    """(admissible, |h - boundary| / r) of the GPU code vg vs oracle vo."""
-    og, oo = _ordered(_bf16_bits([vg, vo]), 0x8000)
-    if abs(int(og) - int(oo)) != 1:
-        return False, np.inf
-    dist = abs(h - 0.5 * (vg + vo))      # the RNE boundary between them
-    return dist <= r, dist / r if r > 0 else np.inf
+def _bf16_of_ordered(o):
+    """Inverse of _ordered for bf16: value of the code at order o."""
+    bits = (0x8000 | -o) if o < 0 else o
+    return float(np.array([bits << 16], dtype=np.uint32).view(np.float32)[0])
 
 
-def _e4m3_neighbours(orc, code):
-    """E4M3 codes next to `code` in value order (NaN codes excluded)."""
-    o = -(code & 0x7F) if code & 0x80 else (code & 0x7F)
-    out = []
-    for n in (o - 1, o + 1):
-        if -126 <= n <= 126:
-            out.append((0x80 | -n) if n < 0 else n)
-    return out
+def _tie_bf16(orc, h, r, vg, vo):
+    """(admissible, code distance, radius use) of the GPU code vg."""
+    rnd = lambda v: orc.bf16_value(orc.bf16_rne(v))   # noqa: E731
+    og, oo = (int(x) for x in _ordered(_bf16_bits([vg, vo]), 0x8000))
+    dist = abs(og - oo)
+    # distance from h to the values that round to vg
+    lo = 0.5 * (vg + _bf16_of_ordered(og - 1))
+    hi = 0.5 * (vg + _bf16_of_ordered(og + 1))
+    gap = (lo - h) if h < lo else (h - hi) if h > hi else 0.0
+    ok = rnd(h - r) <= vg <= rnd(h + r)
+    return ok, dist, (gap / r if r > 0 else np.inf)
 
 
-def _tie_fp8(orc, hgrp, rgrp, idx, vg):
-    """(admissible, |h - boundary| / r) for one element of a 32-group.
+def _e4m3_ordered(c):
+    return -(c & 0x7F) if c & 0x80 else (c & 0x7F)
 
-    Admissible: vg is the E4M3 rounding of h under a group exponent that a
-    maximum within the radius can select, or the adjacent code under that
-    exponent when h lies within r of the boundary between the two."""
+
+def _e4m3_of_ordered(o):
+    return (0x80 | -o) if o < 0 else o
+
+
+def _tie_fp8(orc, hgrp, rgrp, idx, vg, vo):
+    """(admissible, code distance, radius use) for one element of a group.
+
+    Admissible: vg is the E4M3 rounding, under a group exponent that a
+    maximum within the radius can select, of a value within r of h."""
     amax = float(np.abs(hgrp).max())
     rmax = float(rgrp[np.argmax(np.abs(hgrp))])
     lo = orc.fp8_group_exponent(np.full(32, max(amax - rmax, 0.0)))
     hi = orc.fp8_group_exponent(np.full(32, amax + rmax))
     h, r = float(hgrp[idx]), float(rgrp[idx])
-    best = np.inf
     for e in range(lo, hi + 1):
         sc = 2.0 ** e
-        c = orc.e4m3_rne_sat(h / sc)
-        v = orc.e4m3_value(c) * sc
-        if vg == v:
-            return True, 0.0
-        for c2 in _e4m3_neighbours(orc, c):
-            v2 = orc.e4m3_value(c2) * sc
-            if vg == v2:
-                dist = abs(h - 0.5 * (v + v2))
-                best = min(best, dist / r if r > 0 else np.inf)
-    return best <= 1.0, best
+
+        def rnd(v, sc=sc):
+            return orc.e4m3_value(orc.e4m3_rne_sat(v / sc)) * sc
+        if not rnd(h - r) <= vg <= rnd(h + r):
+            continue
+        og = _e4m3_ordered(orc.e4m3_rne_sat(vg / sc))
+        oh = _e4m3_ordered(orc.e4m3_rne_sat(h / sc))
+        if og == oh:            # only the group exponent differs
+            return True, 0, 0.0
+        nb = orc.e4m3_value(_e4m3_of_ordered(og - 1 if og > oh else og + 1)) * sc
+        use = abs(h - 0.5 * (vg + nb)) / r if r > 0 else np.inf
+        return True, abs(og - oh), use
+    return False, -1, np.inf
 
 
 def w2_columns(w, e, cols, gran):
@@ -267,11 +286,12 @@ def check_moe_values(orc, *, K, gran, act_mode, h_gpu, y_gpu, ref_y, ref_h,
     ratio of |error| to the allowed bound in y)."""
     h_gpu = np.asarray(h_gpu, dtype=np.float64)
     h_ref = orc.round_intermediate(ref_h, act_mode).reshape(h_gpu.shape)
-    radius = moe_radius(aux, K)
+    radius = moe_radius(aux)
     mism = np.argwhere(h_gpu != h_ref)
     stats = {"ties": int(len(mism)), "h_elements": int(h_ref.size),
              "tie_frac": len(mism) / max(h_ref.size, 1),
-             "tie_cap": tie_frac, "max_tie_radius_use": 0.0}
+             "tie_cap": tie_frac, "max_tie_radius_use": 0.0,
+             "multi_code_ties": 0, "max_code_distance": 0}
     assert len(mism) <= tie_frac * h_ref.size, (
         f"{what}: h differs from the oracle in {len(mism)} of {h_ref.size} "
         f"elements (cap {tie_frac:g})")
@@ -280,16 +300,18 @@ def check_moe_values(orc, *, K, gran, act_mode, h_gpu, y_gpu, ref_y, ref_h,
         h, r = ref_h[n, j, i], radius[n, j, i]
         vo, vg = h_ref[n, j, i], h_gpu[n, j, i]
         if act_mode == 0:
-            ok, use = _tie_bf16(h, r, vg, vo)
+            ok, dist, use = _tie_bf16(orc, h, r, vg, vo)
         else:
             g0 = (i // 32) * 32
-            ok, use = _tie_fp8(orc, ref_h[n, j, g0:g0 + 32],
-                               radius[n, j, g0:g0 + 32], i - g0, vg)
+            ok, dist, use = _tie_fp8(orc, ref_h[n, j, g0:g0 + 32],
+                                     radius[n, j, g0:g0 + 32], i - g0, vg, vo)
         assert ok, (f"{what}: h[token {n}, slot {j}, {i}] = {vg!r} is not an "
                     f"admissible rounding of {h!r} (radius {r:.3g}, oracle "
                     f"{vo!r})")
         stats["max_tie_radius_use"] = max(stats["max_tie_radius_use"],
                                           float(use))
+        stats["multi_code_ties"] += int(dist > 1)
+        stats["max_code_distance"] = max(stats["max_code_distance"], dist)
         col = w2_columns(w_used, int(ids[n, j]), [int(i)], gran)[:, 0]
         allow[n] += np.abs(wts[n, j] * col * (vg - vo))
     _, err, bound, rms = tolerance_violations(y_gpu, ref_y)

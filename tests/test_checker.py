@@ -1,9 +1,9 @@
 """The MoE parity checker rejects wrong results (CPU only).
 
-The GPU tests accept a differing intermediate h only as the adjacent code of
-the correct rounding, where the exact h lies within the FP32 error radius of
-the boundary between the two, and widen the y tolerance only by the exact
-effect of such ties.  These tests feed the checker the oracle's own result
+The GPU tests accept a differing intermediate h only where it is a correct
+rounding of a value within the FP32 error radius of the exact h (in practice
+the adjacent code, with h next to the boundary between the two), and widen
+the y tolerance only by the exact effect of such ties.  These tests feed the checker the oracle's own result
 (which must pass) and copies of it with planted mistakes (each must fail):
 h two ulps off, a tie far from any boundary, too many ties, one expert's FC2
 output scaled by 1.01, two token rows swapped, and an FP8 code two steps off.
@@ -136,7 +136,7 @@ def test_rejects_h_two_ulps_off_on_2_percent():
 
 
 def test_rejects_h_two_ulps_off_below_the_tie_cap():
-    # three elements only: under the cap, so adjacency alone must catch it
+    # three elements only: under the cap, so the radius alone must catch it
     c = _case(synth.TINY)
     h = c["h_round"].copy()
     for n, j, i in _pick(h, 3 / h.size, 2):
@@ -163,7 +163,7 @@ def test_rejects_too_many_ties(monkeypatch):
     # Every adjacent flip made admissible by an inflated radius: the cap on
     # the number of ties must still reject 2% of h flipped.
     c = _case(synth.TINY)
-    monkeypatch.setattr(_util, "RADIUS_LAMBDA", 1e9)
+    monkeypatch.setattr(_util, "RADIUS_MARGIN", 1e9)
     h = c["h_round"].copy()
     for n, j, i in _pick(h, 0.02, 3):
         h[n, j, i] = _bf16_step(h[n, j, i], 1)
