@@ -210,7 +210,12 @@ class MoeRun:
 
     @property
     def launches_per_step(self) -> int:
-        return 9 if self.fp8 else 7
+        # act_quant, route, scan, scatter, gather, FC1, FC2, combine (FP8: the
+        # block-scaled path rounds h inside FC1; kept group16 weights add the
+        # separate rounding kernel)
+        if self.fp8:
+            return 9 if self.cfg.keep_group16 else 8
+        return 7
 
     def timed(self, steps, warmup, clocks=None):
         torch, fp4 = self.torch, self.fp4

@@ -57,6 +57,9 @@ class PackedDesc(ctypes.Structure):
         ("w2", ctypes.c_void_p), ("w2_bytes", ctypes.c_size_t),
         ("alpha13", ctypes.c_void_p), ("alpha2", ctypes.c_void_p),
         ("scale_mul", ctypes.c_uint32), ("scale_add", ctypes.c_uint32),
+        ("layout", ctypes.c_int32),
+        ("w13_scales", ctypes.c_void_p), ("w13_scales_bytes", ctypes.c_size_t),
+        ("w2_scales", ctypes.c_void_p), ("w2_scales_bytes", ctypes.c_size_t),
     ]
 
 
@@ -282,14 +285,16 @@ class PackedWeights:
         """The packed device buffers as uint8 / float32 torch tensors (copies)."""
         d = self.desc
         out = {}
-        for name, ptr, nbytes in (("w13", d.w13, d.w13_bytes),
-                                  ("w2", d.w2, d.w2_bytes),
-                                  ("alpha13", d.alpha13, 4 * d.E),
-                                  ("alpha2", d.alpha2, 4 * d.E)):
+        items = [("w13", d.w13, d.w13_bytes), ("w2", d.w2, d.w2_bytes),
+                 ("alpha13", d.alpha13, 4 * d.E), ("alpha2", d.alpha2, 4 * d.E)]
+        if d.layout == 1:
+            items += [("w13_scales", d.w13_scales, d.w13_scales_bytes),
+                      ("w2_scales", d.w2_scales, d.w2_scales_bytes)]
+        for name, ptr, nbytes in items:
             host = torch.empty(nbytes, dtype=torch.uint8)
             _memcpy_d2h(host, ptr, nbytes)
-            out[name] = host if name.startswith("w") else host.view(
-                torch.float32)
+            out[name] = host.view(torch.float32) if name.startswith("alpha") \
+                else host
         return out
 
 
@@ -339,14 +344,16 @@ def moe_workspace_size(packed: PackedWeights, T: int, top_k: int) -> int:
 
 
 WS_FIELDS = ("ids", "w", "counts", "offsets", "perm", "inv", "xperm", "h",
-             "o", "total")
+             "o", "total", "h_scales", "h_format", "pitch")
 
 
 def moe_workspace_offsets(packed: PackedWeights, T: int, top_k: int) -> dict:
-    """Byte offsets of moe_forward's intermediates inside its workspace."""
-    arr = (ctypes.c_size_t * 10)()
+    """Byte offsets of moe_forward's intermediates inside its workspace
+    (plus the h format: 0 bf16, 1 E4M3 bytes + scale words of `pitch`)."""
+    n = len(WS_FIELDS)
+    arr = (ctypes.c_size_t * n)()
     _check(load().fp4moe_moe_workspace_offsets(packed.handle, T, top_k, arr,
-                                               10), "moe_workspace_offsets")
+                                               n), "moe_workspace_offsets")
     return dict(zip(WS_FIELDS, list(arr)))
 
 

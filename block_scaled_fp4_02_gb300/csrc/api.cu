@@ -12,10 +12,15 @@ using namespace fp4moe;
 
 struct fp4moe_packed {
   int E, K, I, gran, act_mode, w13_layout, device;
+  bool mx;       // block-scaled path: plain codes + scale words
   uint8_t* w13;
   size_t w13_bytes;
   uint8_t* w2;
   size_t w2_bytes;
+  uint32_t* s13;  // block-scaled path: scale words [E][2I/128][K/128][128]
+  size_t s13_bytes;
+  uint32_t* s2;   //                    [E][K/128][I/128][128]
+  size_t s2_bytes;
   float* alpha;  // [2E]: FC1 then FC2
   uint32_t smul, sadd;
 };
@@ -66,6 +71,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Row-major [rows, cols] of E2M1 codes (two per byte) read in 128 x 128
+// boxes with the 16U4_ALIGN16B type (each 16 codes widened to 16 bytes in
+// shared memory) and the 128-byte swizzle: the kind::mxf8f6f4 operand form.
+bool make_e2m1_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols / 2};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major bytes [rows, cols] (E4M3) read in boxes of box_rows x 128 with
+// the 128-byte swizzle.
+bool make_u8_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major bf16 [rows, cols] read in boxes of box_rows rows x 64 columns
 // with the 128-byte swizzle (the UMMA K-major operand layout).
 bool make_row_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -99,8 +134,13 @@ RouteLayout route_layout(int T, int E, size_t start = 0) {
 
 struct MoeLayout {
   RouteLayout r;
-  size_t ids, wts, counts, offsets, perm, inv, xperm, h, h32, o, total;
+  size_t ids, wts, counts, offsets, perm, inv, xperm, xs, h, hs, h32, o, total;
+  int64_t pitch;  // block-scaled path: scale words per step row
 };
+
+// Words per step row of the block-scaled path's scale arrays: P rounded up
+// to 4 plus the over-read of the aligned bulk copies of the last chunk.
+int64_t mx_pitch(int64_t P) { return ((P + 3) & ~3LL) + 264; }
 
 MoeLayout moe_layout(const fp4moe_packed* p, int T, int k) {
   const size_t P = static_cast<size_t>(T) * k;
@@ -114,9 +154,19 @@ MoeLayout moe_layout(const fp4moe_packed* p, int T, int k) {
   L.offsets = take((static_cast<size_t>(p->E) + 1) * 4);
   L.perm = take(P * 4);
   L.inv = take(P * 4);
-  L.xperm = take(P * p->K * 2);
-  L.h = take(P * p->I * 2);
-  L.h32 = (p->act_mode == FP4MOE_ACT_FP8) ? take(P * p->I * 4) : 0;
+  L.pitch = 0;
+  L.xs = L.hs = L.h32 = 0;
+  if (p->mx) {
+    L.pitch = mx_pitch(static_cast<int64_t>(P));
+    L.xperm = take(P * p->K);
+    L.xs = take(static_cast<size_t>(p->K / kMxK) * L.pitch * 4);
+    L.h = take(P * p->I);
+    L.hs = take(static_cast<size_t>(p->I / kMxK) * L.pitch * 4);
+  } else {
+    L.xperm = take(P * p->K * 2);
+    L.h = take(P * p->I * 2);
+    L.h32 = (p->act_mode == FP4MOE_ACT_FP8) ? take(P * p->I * 4) : 0;
+  }
   L.o = take(P * p->K * 4);
   L.total = off;
   return L;
@@ -138,8 +188,80 @@ void free_packed(fp4moe_packed* p) {
   if (!p) return;
   cudaFree(p->w13);
   cudaFree(p->w2);
+  cudaFree(p->s13);
+  cudaFree(p->s2);
   cudaFree(p->alpha);
   delete p;
+}
+
+// The MoE layer on the block-scaled path (FP8 activations over group32
+// weights): routing, permutation, gather of the E4M3 rows and their scale
+// words, FC1 + SwiGLU with the FP8 rounding of h in its epilogue, FC2 and the
+// combine; stage events as in fp4moe_moe_forward (no separate rounding of h,
+// so events 4 and 5 coincide).
+int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void* x,
+               const uint8_t* x_scales, const float* router_logits, int T, int top_k,
+               void* y, cudaStream_t st) {
+  auto at = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  int32_t *hist = at(L.r.hist), *base = at(L.r.base), *cstart = at(L.r.cstart);
+  int32_t *ids = at(L.ids), *counts = at(L.counts), *offsets = at(L.offsets);
+  int32_t *perm = at(L.perm), *inv = at(L.inv);
+  float* wts = reinterpret_cast<float*>(ws + L.wts);
+  uint8_t* xperm = reinterpret_cast<uint8_t*>(ws + L.xperm);
+  uint32_t* xs = reinterpret_cast<uint32_t*>(ws + L.xs);
+  uint8_t* h8 = reinterpret_cast<uint8_t*>(ws + L.h);
+  uint32_t* hs = reinterpret_cast<uint32_t*>(ws + L.hs);
+  float* o = reinterpret_cast<float*>(ws + L.o);
+  int* err = status_word();
+  const int64_t P = static_cast<int64_t>(T) * top_k;
+  const int sms = device_sm_count();
+  struct StageOff {
+    ~StageOff() { t_stage_on = false; }
+  } stage_off;
+  stage_mark(0, st);
+  cudaError_t e = launch_route(router_logits, T, p->E, top_k, ids, wts, hist, err, st);
+  stage_mark(1, st);
+  if (e == cudaSuccess)
+    e = launch_scan(T, p->E, hist, base, counts, offsets, cstart, kMxChunk, st);
+  stage_mark(2, st);
+  if (e == cudaSuccess)
+    e = launch_scatter(ids, T, p->E, top_k, base, perm, inv, nullptr, nullptr, 0,
+                       FP4MOE_ACT_FP8, nullptr, st);
+  if (e == cudaSuccess)
+    e = launch_gather_mx(inv, T, top_k, static_cast<const uint8_t*>(x), x_scales, p->K,
+                         L.pitch, xperm, xs, st);
+  stage_mark(3, st);
+  if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+
+  CUtensorMap m1[5], m2[5];
+  const uint32_t boxes[4] = {64, 128, 192, 256};
+  bool ok = make_e2m1_tmap(&m1[0], p->w13, static_cast<uint64_t>(p->E) * 2 * p->I, p->K) &&
+            make_e2m1_tmap(&m2[0], p->w2, static_cast<uint64_t>(p->E) * p->K, p->I);
+  for (int i = 0; i < 4 && ok; ++i)
+    ok = make_u8_tmap(&m1[1 + i], xperm, P, p->K, boxes[i]) &&
+         make_u8_tmap(&m2[1 + i], h8, P, p->I, boxes[i]);
+  if (!ok) return FP4MOE_ERR_CUDA;
+  MxGemmArgs a1{};
+  a1.wscale = p->s13; a1.xscale = xs; a1.alpha = p->alpha; a1.offsets = offsets;
+  a1.cstart = cstart; a1.out = h8; a1.hscale = reinterpret_cast<uint8_t*>(hs); a1.err = err;
+  a1.E = p->E; a1.nblocks = p->I / 128; a1.ksteps = p->K / kMxK;
+  a1.rows_per_expert = 2 * p->I; a1.tiles_per_expert = 2 * p->I / 128;
+  a1.xscale_pitch = L.pitch; a1.hscale_pitch = L.pitch; a1.ldo = p->I;
+  a1.mode = kGemmModeFc1;
+  e = launch_gemm_mx(m1, a1, sms, st);
+  stage_mark(4, st);
+  stage_mark(5, st);
+  MxGemmArgs a2 = a1;
+  a2.wscale = p->s2; a2.xscale = hs; a2.alpha = p->alpha + p->E; a2.out = o;
+  a2.hscale = nullptr; a2.nblocks = p->K / 128; a2.ksteps = p->I / kMxK;
+  a2.rows_per_expert = p->K; a2.tiles_per_expert = p->K / 128; a2.ldo = p->K;
+  a2.mode = kGemmModeFc2;
+  if (e == cudaSuccess) e = launch_gemm_mx(m2, a2, sms, st);
+  stage_mark(6, st);
+  if (e == cudaSuccess)
+    e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), st);
+  stage_mark(7, st);
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -271,17 +393,29 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
   const bool requant = (mode == FP4MOE_ACT_FP8 && gran_k == 16 && !keep16);
   if (requant && no_requant) return FP4MOE_ERR_UNSUPPORTED;
   const int g = requant ? 32 : gran_k;
+  // FP8 activations over group32 weights (given, or from the requant) run
+  // on the block-scaled tensor-core path; kept group16 weights and bf16
+  // activations on the bf16 path.
+  const bool mx = (mode == FP4MOE_ACT_FP8 && g == 32);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   fp4moe_packed* p = new fp4moe_packed{};
   p->E = E; p->K = K; p->I = I; p->gran = g; p->act_mode = mode;
   p->w13_layout = w13_layout;
+  p->mx = mx;
   cudaGetDevice(&p->device);
-  p->smul = (g == 16) ? 16u : 128u;
-  p->sadd = (g == 16) ? 0x7680u : 0u;
+  p->smul = mx ? 0u : (g == 16) ? 16u : 128u;
+  p->sadd = (!mx && g == 16) ? 0x7680u : 0u;
   const int64_t n13 = 2LL * I, n2 = K;
-  p->w13_bytes = static_cast<size_t>(E) * (n13 / kTileN) * (K / kTileK) * tile_bytes(g);
-  p->w2_bytes = static_cast<size_t>(E) * (n2 / kTileN) * (I / kTileK) * tile_bytes(g);
+  if (mx) {
+    p->w13_bytes = static_cast<size_t>(E) * n13 * (K / 2);
+    p->w2_bytes = static_cast<size_t>(E) * n2 * (I / 2);
+    p->s13_bytes = static_cast<size_t>(E) * n13 * (K / kMxK) * 4;
+    p->s2_bytes = static_cast<size_t>(E) * n2 * (I / kMxK) * 4;
+  } else {
+    p->w13_bytes = static_cast<size_t>(E) * (n13 / kTileN) * (K / kTileK) * tile_bytes(g);
+    p->w2_bytes = static_cast<size_t>(E) * (n2 / kTileN) * (I / kTileK) * tile_bytes(g);
+  }
 
   uint8_t* tmp = nullptr;   // requant output, if any
   int32_t* bmax = nullptr;  // [2E]
@@ -296,6 +430,8 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
   };
   if (cudaMalloc(&p->w13, p->w13_bytes) != cudaSuccess ||
       cudaMalloc(&p->w2, p->w2_bytes) != cudaSuccess ||
+      (mx && cudaMalloc(&p->s13, p->s13_bytes) != cudaSuccess) ||
+      (mx && cudaMalloc(&p->s2, p->s2_bytes) != cudaSuccess) ||
       cudaMalloc(&p->alpha, 2 * E * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&bmax, 2 * E * sizeof(int32_t)) != cudaSuccess ||
       cudaMalloc(&err, sizeof(int)) != cudaSuccess)
@@ -325,18 +461,32 @@ int fp4moe_prepare_weights(const uint8_t* w13, const uint8_t* w13_s,
       e = launch_requant(w2, w2_s, static_cast<int64_t>(E) * n2, I, rc2, rs2, err, st);
     c13 = rc13; s13 = rs13; c2 = rc2; s2 = rs2;
   }
-  if (e == cudaSuccess && g == 32) {
-    e = launch_scale_max(s13, E, n13 * (K / 32), bmax, err, st);
-    if (e == cudaSuccess) e = launch_scale_max(s2, E, n2 * (I / 32), bmax + E, err, st);
+  if (mx) {
+    // Plain codes (FC1 rows reordered into gate/up tiles) and scale words.
+    if (e == cudaSuccess)
+      e = launch_mx_rows(c13, E, static_cast<int>(n13), K, true, w13_layout, p->w13, st);
+    if (e == cudaSuccess)
+      e = launch_mx_rows(c2, E, static_cast<int>(n2), I, false, 0, p->w2, st);
+    if (e == cudaSuccess)
+      e = launch_mx_scales(s13, E, static_cast<int>(n13), K, true, w13_layout, p->s13, err, st);
+    if (e == cudaSuccess)
+      e = launch_mx_scales(s2, E, static_cast<int>(n2), I, false, 0, p->s2, err, st);
+    if (e == cudaSuccess) e = launch_alpha(w13_gs, nullptr, E, 0, gs_inv, p->alpha, st);
+    if (e == cudaSuccess) e = launch_alpha(w2_gs, nullptr, E, 0, gs_inv, p->alpha + E, st);
+  } else {
+    if (e == cudaSuccess && g == 32) {
+      e = launch_scale_max(s13, E, n13 * (K / 32), bmax, err, st);
+      if (e == cudaSuccess) e = launch_scale_max(s2, E, n2 * (I / 32), bmax + E, err, st);
+    }
+    if (e == cudaSuccess)
+      e = launch_pack(c13, s13, E, static_cast<int>(n13), K, g, true, w13_layout, bmax,
+                      p->w13, err, st);
+    if (e == cudaSuccess)
+      e = launch_pack(c2, s2, E, static_cast<int>(n2), I, g, false, 0, bmax + E, p->w2,
+                      err, st);
+    if (e == cudaSuccess) e = launch_alpha(w13_gs, bmax, E, g, gs_inv, p->alpha, st);
+    if (e == cudaSuccess) e = launch_alpha(w2_gs, bmax + E, E, g, gs_inv, p->alpha + E, st);
   }
-  if (e == cudaSuccess)
-    e = launch_pack(c13, s13, E, static_cast<int>(n13), K, g, true, w13_layout, bmax,
-                    p->w13, err, st);
-  if (e == cudaSuccess)
-    e = launch_pack(c2, s2, E, static_cast<int>(n2), I, g, false, 0, bmax + E, p->w2,
-                    err, st);
-  if (e == cudaSuccess) e = launch_alpha(w13_gs, bmax, E, g, gs_inv, p->alpha, st);
-  if (e == cudaSuccess) e = launch_alpha(w2_gs, bmax + E, E, g, gs_inv, p->alpha + E, st);
   if (e != cudaSuccess) return fail(FP4MOE_ERR_CUDA);
   if (cudaStreamSynchronize(st) != cudaSuccess) return fail(FP4MOE_ERR_CUDA);
   int h_err = 0;
@@ -360,11 +510,15 @@ int fp4moe_packed_info(const fp4moe_packed* p, fp4moe_packed_desc* d) {
   if (!p || !d) return FP4MOE_ERR_INVALID_ARG;
   d->E = p->E; d->K = p->K; d->I = p->I; d->gran_k = p->gran;
   d->act_mode = p->act_mode; d->w13_layout = p->w13_layout;
-  d->k_tile = kTileK; d->n_tile = kTileN; d->tile_bytes = tile_bytes(p->gran);
+  d->k_tile = p->mx ? kMxK : kTileK; d->n_tile = kTileN;
+  d->tile_bytes = p->mx ? 0 : tile_bytes(p->gran);
   d->w13 = p->w13; d->w13_bytes = p->w13_bytes;
   d->w2 = p->w2; d->w2_bytes = p->w2_bytes;
   d->alpha13 = p->alpha; d->alpha2 = p->alpha + p->E;
   d->scale_mul = p->smul; d->scale_add = p->sadd;
+  d->layout = p->mx ? 1 : 0;
+  d->w13_scales = p->s13; d->w13_scales_bytes = p->s13_bytes;
+  d->w2_scales = p->s2; d->w2_scales_bytes = p->s2_bytes;
   return FP4MOE_OK;
 }
 
@@ -379,9 +533,10 @@ int fp4moe_moe_workspace_offsets(const fp4moe_packed* p, int T, int top_k,
       top_k > std::min(p->E, kMaxTopK))
     return FP4MOE_ERR_INVALID_ARG;
   const MoeLayout L = moe_layout(p, T, top_k);
-  const size_t v[10] = {L.ids, L.wts, L.counts, L.offsets, L.perm,
-                        L.inv, L.xperm, L.h, L.o, L.total};
-  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  const size_t v[13] = {L.ids, L.wts, L.counts, L.offsets, L.perm,
+                        L.inv, L.xperm, L.h, L.o, L.total,
+                        L.hs, p->mx ? 1u : 0u, static_cast<size_t>(L.pitch)};
+  for (int i = 0; i < std::min(n, 13); ++i) out[i] = v[i];
   return FP4MOE_OK;
 }
 
@@ -395,6 +550,7 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   if (!x || !router_logits || !y || !workspace) return FP4MOE_ERR_INVALID_ARG;
   if (p->act_mode == FP4MOE_ACT_BF16 && x_scales) return FP4MOE_ERR_INVALID_ARG;
   if (p->act_mode == FP4MOE_ACT_FP8 && !x_scales) return FP4MOE_ERR_INVALID_ARG;
+  if (p->mx && !aligned(x_scales, 4)) return FP4MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, kAlign))
     return FP4MOE_ERR_INVALID_ARG;
   int dev = 0;
@@ -410,6 +566,7 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   int32_t *ids = at(L.ids), *counts = at(L.counts), *offsets = at(L.offsets);
   int32_t *perm = at(L.perm), *inv = at(L.inv);
   float* wts = reinterpret_cast<float*>(ws + L.wts);
+  if (p->mx) return mx_forward(p, L, ws, x, x_scales, router_logits, T, top_k, y, st);
   uint16_t* xperm = reinterpret_cast<uint16_t*>(ws + L.xperm);
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
   float* h32 = reinterpret_cast<float*>(ws + L.h32);

@@ -175,6 +175,43 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// D(tmem) (+)= (A(smem) x SFA) * (B(smem) x SFB)^T, kind::mxf8f6f4 with
+// block scaling: one UE8M0 scale per 32 K elements of each row of A and of
+// B, read from TMEM.  A row m's scale sits in lane m, column m / 32 of the
+// SFA address; B row n's scale in column n / 32, lane n % 32 of every lane
+// quarter (each quarter of the accumulator rows reads its own copy); the
+// byte within the 32-bit column is the instruction descriptor's scale id.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc,
+                                        uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 bits, one column per thread (store).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+               "r"(r)
+               : "memory");
+}
+
+// 32 lanes x 32 bits, 8 consecutive columns per thread (store).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7])
+      : "memory");
+}
+
 // 32 lanes x 32 bits, 16 consecutive columns per thread (store).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -260,6 +297,16 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// Instruction descriptor, kind::mxf8f6f4 with UE8M0 block scales: A E2M1,
+// B E4M3, D f32, both K-major; sfa_id / sfb_id pick the byte of the scale
+// columns (the 32-wide K block within a 128-wide step).
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(uint32_t M, uint32_t N,
+                                                         uint32_t sfa_id,
+                                                         uint32_t sfb_id) {
+  return (sfb_id << 4) | (5u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) |
+         ((M >> 4) << 24) | (sfa_id << 29);
+}
+
 // Instruction descriptor, kind::f16: A = B = bf16, D = f32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) |
@@ -334,6 +381,25 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v) {
       : "r"(v & 0xFFFFu));
   __half2 hh = *reinterpret_cast<__half2*>(&h);
   return __half22float2(hh);
+}
+
+// UE8M0 byte of the FP8 recipe (1,1,32): e = min{e : amax <= 448 * 2^e},
+// byte e + 127 clamped to [0, 254]; amax = 0 gives 127.
+__device__ __forceinline__ uint32_t ue8m0_for_e4m3(float amax) {
+  if (!(amax > 0.0f)) return 127u;
+  const uint32_t bits = __float_as_uint(amax);
+  const int field = static_cast<int>(bits >> 23);
+  if (field == 0) return 0u;  // below 2^-126: the clamp gives byte 0
+  const int E = field - 127;
+  // 448 = 1.75 * 2^8: 448 * 2^(E-8) covers mantissas up to 1.75.
+  const int e = ((bits & 0x7FFFFFu) <= 0x600000u) ? E - 8 : E - 7;
+  return static_cast<uint32_t>(max(0, min(254, e + 127)));
+}
+
+// 2^e as f32 for e in [-149, 127].
+__device__ __forceinline__ float pow2_any(int e) {
+  return (e >= -126) ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                     : __uint_as_float(1u << (e + 149));
 }
 
 // 2^e as f32 for e in [-126, 127].

@@ -66,7 +66,8 @@ cudaError_t launch_pack(const uint8_t* w, const uint8_t* s, int E, int N,
                         const int32_t* bmax, uint8_t* out, int* err,
                         cudaStream_t st);
 // alpha = gs (or 1 / gs when the global scales are stored inverted) times
-// the power of two that the packed scale codes leave out.
+// the power of two that the packed scale codes leave out (gran 16, 32);
+// gran 0: gs alone (block-scaled path, whose scales the MMA applies).
 cudaError_t launch_alpha(const float* gs, const int32_t* bmax, int E,
                          int gran, bool inverted, float* alpha, cudaStream_t st);
 
@@ -89,6 +90,44 @@ constexpr int kGemmModeFc1 = 0, kGemmModeFc2 = 1, kGemmModeFc1Fp8 = 2;
 
 cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
                         int num_sms, cudaStream_t st);
+
+// S5 / S6 on the block-scaled path (FP8 activations over group32 weights):
+// kind::mxf8f6f4, E2M1 weights widened by TMA, E4M3 rows, UE8M0 scales.
+constexpr int kMxK = 128;             // K elements per step
+constexpr int kMxChunk = 224;         // tokens per unit (accumulator columns)
+constexpr int kMxChunk256Rows = 256;  // largest activation box (rows)
+constexpr int kMxSfSlots = 2;         // scale-factor slots in TMEM
+struct MxGemmArgs {
+  const uint32_t* wscale;  // [E][tiles][ksteps][128] UE8M0 words (4 blocks)
+  const uint32_t* xscale;  // [ksteps][xscale_pitch] words of the B rows
+  const float* alpha;      // [E] epilogue scale (global scale)
+  const int32_t* offsets;  // [E+1] token offsets (expert-major rows)
+  const int32_t* cstart;   // [E+1] token-chunk prefix (chunks <= kMxChunk)
+  void* out;               // FC1: h E4M3 [P, ldo]; FC2: o f32 [P, ldo]
+  uint8_t* hscale;         // FC1: h scale words [I/128][hscale_pitch]
+  int* err;
+  int E, nblocks, ksteps, rows_per_expert, tiles_per_expert;
+  int64_t xscale_pitch, hscale_pitch;  // words per step row
+  int ldo;
+  int mode;                // kGemmModeFc1 (SwiGLU, FP8 h) or kGemmModeFc2
+};
+// S0 of the block-scaled path: rows of one weight matrix [E, N, Kd/2] copied
+// (FC1 reordered: per 128-column block the gate rows then the up rows), and
+// its UE8M0 scales [E, N, Kd/32] regrouped as one word per row and 128-wide
+// step, [E][N/128][Kd/128][128].
+cudaError_t launch_mx_rows(const uint8_t* w, int E, int N, int Kd, bool gated, int layout,
+                           uint8_t* out, cudaStream_t st);
+cudaError_t launch_mx_scales(const uint8_t* s, int E, int N, int Kd, bool gated, int layout,
+                             uint32_t* out, int* err, cudaStream_t st);
+// S3 gather of the block-scaled path: E4M3 rows to xperm [P, K] and their
+// scale words to xsperm [K/128][pitch].
+cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
+                             const uint8_t* xs, int K, int64_t pitch, uint8_t* xperm,
+                             uint32_t* xsperm, cudaStream_t st);
+// maps: weights (16U4_ALIGN16B, 128 x 128 boxes), then the activation rows
+// with boxes of 64, 128, 192 and 256 rows (E4M3, 128-byte swizzle).
+cudaError_t launch_gemm_mx(const CUtensorMap (&maps)[5], const MxGemmArgs& a,
+                           int num_sms, cudaStream_t st);
 
 // Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
 int gemm_chunk_max(int T);

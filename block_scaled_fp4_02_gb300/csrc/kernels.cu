@@ -158,17 +158,6 @@ __global__ void __launch_bounds__(256) requant_kernel(
 // Recipe (1,1,32) of the group16 notes page: per token and 32 consecutive K
 // elements, UE8M0 e = min{e : amax <= 448 * 2^e}, q = E4M3(x / 2^e).
 
-__device__ __forceinline__ uint32_t ue8m0_for_e4m3(float amax) {
-  if (!(amax > 0.0f)) return 127u;
-  const uint32_t bits = __float_as_uint(amax);
-  const int field = static_cast<int>(bits >> 23);
-  if (field == 0) return 0u;  // below 2^-126: the clamp gives byte 0
-  const int E = field - 127;
-  // 448 = 1.75 * 2^8: 448 * 2^(E-8) covers mantissas up to 1.75.
-  const int e = ((bits & 0x7FFFFFu) <= 0x600000u) ? E - 8 : E - 7;
-  return static_cast<uint32_t>(max(0, min(254, e + 127)));
-}
-
 __global__ void __launch_bounds__(256) act_quant_kernel(
     const uint16_t* __restrict__ x, int64_t groups, uint8_t* __restrict__ q,
     uint8_t* __restrict__ s, int* err) {
@@ -212,11 +201,6 @@ __global__ void __launch_bounds__(256) act_quant_kernel(
 // FP8 rounding of the FC1 output h (FP8 activation path): per row and 32
 // consecutive columns, the same UE8M0 + E4M3 rule as the activation
 // quantization, stored back as the exact bf16 value q * 2^e for FC2.
-__device__ __forceinline__ float pow2_any(int e) {  // 2^e, e in [-149, 127]
-  return (e >= -126) ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
-                     : __uint_as_float(1u << (e + 149));
-}
-
 __global__ void __launch_bounds__(256) h_fp8_round_kernel(
     const float* __restrict__ h, int64_t groups, uint16_t* __restrict__ out) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -627,7 +611,84 @@ __global__ void alpha_kernel(const float* __restrict__ gs,
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const float g = inverted ? 1.0f / gs[e] : gs[e];   // IEEE division
-  alpha[e] = (gran == 16) ? g * 128.0f : ldexpf(g, bmax[e] - 128);
+  alpha[e] = (gran == 16) ? g * 128.0f : (gran == 32) ? ldexpf(g, bmax[e] - 128) : g;
+}
+
+// ============================================= block-scaled (FP8 x FP4) path
+//
+// Weights for kind::mxf8f6f4 stay plain E2M1 codes, two per byte (the TMA
+// widens them on the way into shared memory); only the rows are reordered
+// and the UE8M0 scales regrouped.  FC1 rows of block b (128 intermediate
+// columns): gate rows 128 b .. 128 b + 127 at 256 b, the up rows of the same
+// columns at 256 b + 128.  Scale words: one 32-bit word per row and 128-wide
+// K step holding the four UE8M0 bytes of its 32-wide blocks, ordered
+// [expert][128-row tile][step][row].
+
+// One block per destination row (gated: reordered), 16 bytes per thread.
+__global__ void __launch_bounds__(256) mx_rows_kernel(
+    const uint8_t* __restrict__ w, int N, int64_t row_bytes, int gated,
+    int layout, uint8_t* __restrict__ out) {
+  const int64_t R = blockIdx.x;                  // destination row (all experts)
+  const int e = static_cast<int>(R / N), r = static_cast<int>(R % N);
+  int src = r;
+  if (gated) {
+    const int I = N / 2, b = r >> 8, t = (r >> 7) & 1, rr = r & 127;
+    const int gate0 = (layout == FP4MOE_W13_GATE_UP) ? 0 : I;
+    const int up0 = (layout == FP4MOE_W13_GATE_UP) ? I : 0;
+    src = (t ? up0 : gate0) + 128 * b + rr;
+  }
+  const uint4* s4 = reinterpret_cast<const uint4*>(w + (static_cast<int64_t>(e) * N + src) * row_bytes);
+  uint4* d4 = reinterpret_cast<uint4*>(out + R * row_bytes);
+  for (int64_t c = threadIdx.x; c < row_bytes / 16; c += blockDim.x) d4[c] = s4[c];
+}
+
+// One thread per (expert, destination row, step): four scale bytes -> word.
+__global__ void __launch_bounds__(256) mx_scales_kernel(
+    const uint8_t* __restrict__ s, int E, int N, int ksteps, int gated,
+    int layout, uint32_t* __restrict__ out, int* err) {
+  const int64_t n = static_cast<int64_t>(E) * N * ksteps;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(idx % 128);
+    const int64_t rest = idx / 128;
+    const int ks = static_cast<int>(rest % ksteps);
+    const int64_t tg = rest / ksteps;            // tile over all experts
+    const int tiles = N / 128;
+    const int e = static_cast<int>(tg / tiles), tile = static_cast<int>(tg % tiles);
+    const int R = 128 * tile + r;                 // destination row in the expert
+    int src = R;
+    if (gated) {
+      const int I = N / 2, b = R >> 8, t = (R >> 7) & 1, rr = R & 127;
+      const int gate0 = (layout == FP4MOE_W13_GATE_UP) ? 0 : I;
+      const int up0 = (layout == FP4MOE_W13_GATE_UP) ? I : 0;
+      src = (t ? up0 : gate0) + 128 * b + rr;
+    }
+    const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(
+        s + (static_cast<int64_t>(e) * N + src) * (4 * ksteps)) + ks);
+    // UE8M0 0xFF is NaN: reject.
+    if (((word & 0xFFu) == 0xFFu) || (((word >> 8) & 0xFFu) == 0xFFu) ||
+        (((word >> 16) & 0xFFu) == 0xFFu) || ((word >> 24) == 0xFFu))
+      record_error(err, FP4MOE_ERR_INVALID_ARG);
+    out[idx] = word;
+  }
+}
+
+// Activation gather of the block-scaled path: row p of the pair list goes to
+// expert-major slot inv[p] as E4M3 bytes, and its UE8M0 scale words to
+// xs_perm[step][inv[p]].
+__global__ void __launch_bounds__(256) gather_mx_kernel(
+    const int32_t* __restrict__ inv, int64_t P, int k, const uint8_t* __restrict__ x,
+    const uint8_t* __restrict__ xs, int K, int64_t pitch, uint8_t* __restrict__ xperm,
+    uint32_t* __restrict__ xsperm) {
+  for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
+    const int64_t t = p / k;
+    const int64_t row = inv[p];
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
+    uint4* dst = reinterpret_cast<uint4*>(xperm + row * K);
+    for (int c = threadIdx.x; c < K / 16; c += blockDim.x) dst[c] = __ldg(src + c);
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(xs + t * (K / 32));
+    for (int c = threadIdx.x; c < K / 128; c += blockDim.x) xsperm[c * pitch + row] = __ldg(sw + c);
+  }
 }
 
 }  // namespace
@@ -714,6 +775,36 @@ cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
   const int64_t P = static_cast<int64_t>(T) * k;
   const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
   gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_rows(const uint8_t* w, int E, int N, int Kd, bool gated, int layout,
+                           uint8_t* out, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(E) * N;
+  if (rows == 0) return cudaSuccess;
+  if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  mx_rows_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(w, N, Kd / 2, gated ? 1 : 0,
+                                                              layout, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_scales(const uint8_t* s, int E, int N, int Kd, bool gated, int layout,
+                             uint32_t* out, int* err, cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(E) * N * (Kd / kMxK);
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, num_sms() * 8));
+  mx_scales_kernel<<<blocks, 256, 0, st>>>(s, E, N, Kd / kMxK, gated ? 1 : 0, layout, out,
+                                           err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
+                             const uint8_t* xs, int K, int64_t pitch, uint8_t* xperm,
+                             uint32_t* xsperm, cudaStream_t st) {
+  const int64_t P = static_cast<int64_t>(T) * k;
+  if (P == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
+  gather_mx_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, pitch, xperm, xsperm);
   return cudaGetLastError();
 }
 

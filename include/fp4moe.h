@@ -89,6 +89,19 @@ typedef struct fp4moe_packed_desc {
   const float* alpha13;          /* device [E]: FC1 epilogue scale          */
   const float* alpha2;           /* device [E]: FC2 epilogue scale          */
   uint32_t scale_mul, scale_add; /* scale code c -> bf16 bits c*mul + add   */
+  /* layout 0: tiles of 128 rows x 64 K with scale codes (bf16 path);
+   * layout 1: block-scaled path (FP8 activations over group32 weights):
+   *   w13 [E][2I][K/2] plain E2M1 codes, rows per 128-column block b: the
+   *   gate rows of columns 128b..128b+127 at 256b, their up rows at
+   *   256b+128; w2 [E][K][I/2] as given; w13_scales / w2_scales: one 32-bit
+   *   word per row and 128-wide K step holding its four UE8M0 bytes (block
+   *   j of the step in byte j), ordered [E][rows/128][K/128][128]; alpha is
+   *   the global scale (gs, or 1/gs with FP4MOE_FLAG_GS_INVERTED). */
+  int32_t layout;
+  const uint32_t* w13_scales;
+  size_t w13_scales_bytes;
+  const uint32_t* w2_scales;
+  size_t w2_scales_bytes;
 } fp4moe_packed_desc;
 
 /* ------------------------------------------------------------------ S1 --
@@ -130,8 +143,12 @@ int fp4moe_act_quant(const void* x_bf16, int64_t T, int64_t K, uint8_t* xq,
  *   w2  [E, K, I/2]  codes, w2_s  [E, K, I/gran_k],  w2_gs  [E] FP32.
  * gran_k 16 -> E4M3 scales, 32 -> UE8M0 scales.  act_mode FP4MOE_ACT_BF16
  * or FP4MOE_ACT_FP8, optionally OR FP4MOE_FLAG_NO_REQUANT or
- * FP4MOE_FLAG_KEEP_GROUP16, and FP4MOE_FLAG_GS_INVERTED.  With FP8 and gran_k 16 the weights are
- * requantized to group32 first (lossy, as above) unless KEEP_GROUP16 is set.
+ * FP4MOE_FLAG_KEEP_GROUP16, and FP4MOE_FLAG_GS_INVERTED.  With FP8 and
+ * gran_k 16 the weights are requantized to group32 first (lossy, as above)
+ * unless KEEP_GROUP16 is set.  FP8 activations over group32 weights (given,
+ * or from that requant) run on the block-scaled tensor-core path
+ * (kind::mxf8f6f4 with UE8M0 scales in TMEM, layout 1 of the description);
+ * bf16 activations and kept group16 weights run on the bf16 path.
  * Requires K % 128 == 0, I % 128 == 0, E >= 1.
  * SYNCHRONOUS: allocates device memory for the packed weights, runs the
  * packing kernels on `stream`, synchronises it, and returns INVALID_ARG if a
@@ -206,9 +223,14 @@ int fp4moe_moe_forward_host(const void* x_host, const uint8_t* x_scales_host,
  * top_k), of its intermediates, so a test can read them back after a call:
  * out[0] ids int32 [T*top_k], [1] routing weights FP32 [T*top_k], [2] counts
  * int32 [E], [3] offsets int32 [E+1], [4] perm int32 [P], [5] inv int32 [P],
- * [6] gathered activations bf16 [P, K], [7] h bf16 [P, I] (FC2's input, in
- * expert-major order), [8] FC2 output FP32 [P, K], [9] total size.  n >= 10
- * (host array); INVALID_ARG otherwise. */
+ * [6] gathered activations [P, K] (bf16; E4M3 bytes on the block-scaled
+ * path), [7] h [P, I] (FC2's input, in expert-major order: bf16 values, or
+ * E4M3 bytes on the block-scaled path), [8] FC2 output FP32 [P, K], [9] total
+ * size; with n >= 13 also [10] the block-scaled path's h scale words
+ * [I/128][pitch] (word row p holds the four UE8M0 bytes of h row p's 32-wide
+ * groups in that 128-column step; 0 otherwise), [11] the h format (0 bf16,
+ * 1 E4M3 bytes + scale words), [12] that pitch in words.  n >= 10 (host
+ * array); INVALID_ARG otherwise. */
 int fp4moe_moe_workspace_offsets(const fp4moe_packed* p, int T, int top_k,
                                  size_t* out, int n);
 

@@ -118,6 +118,31 @@ def decode_packed(buf: np.ndarray, E, N, Kd, gran, smul, sadd, alpha,
     return out
 
 
+def decode_packed_mx(codes, words, E, N, Kd, alpha, gated, I=None, layout=0):
+    """Block-scaled layout -> dequantized weights [E, N, Kd] in source row
+    order.  codes: [E][N][Kd/2] bytes with FC1 rows reordered (per 128-column
+    block b: gate rows at 256 b, up rows at 256 b + 128); words: one 32-bit
+    word per row and 128-wide step, [E][N/128][Kd/128][128], byte j = UE8M0
+    of the step's j-th 32-wide block."""
+    c = codes[: E * N * Kd // 2].reshape(E, N, Kd // 2)
+    lo, hi = c & 0xF, c >> 4
+    e2m1 = E2M1[np.stack([lo, hi], -1).reshape(E, N, Kd)]
+    w = words[: E * N * Kd // 32].copy().reshape(E, N // 128, Kd // 128, 128, 4)
+    sbytes = w.transpose(0, 1, 3, 2, 4).reshape(E, N, Kd // 32).astype(np.int64)
+    val = e2m1 * np.repeat(np.ldexp(1.0, sbytes - 127), 32, axis=-1)
+    val = val * alpha.astype(np.float64)[:, None, None]
+    out = np.empty((E, N, Kd))
+    R = np.arange(N)
+    if gated:
+        b, t, r = R // 256, (R // 128) % 2, R % 128
+        gate0, up0 = (0, I) if layout == 0 else (I, 0)
+        src = np.where(t == 0, gate0, up0) + 128 * b + r
+    else:
+        src = R
+    out[:, src, :] = val
+    return out
+
+
 def dequant_reference(codes_packed, scales, gran, gs):
     """Plain decode of raw [E, N, Kd/2] codes + [E, N, Kd/g] scales."""
     lo, hi = codes_packed & 0xF, codes_packed >> 4
@@ -247,7 +272,8 @@ def _tie_fp8(orc, hgrp, rgrp, idx, vg, vo):
 
         def rnd(v, sc=sc):
             return orc.e4m3_value(orc.e4m3_rne_sat(v / sc)) * sc
-        if not rnd(h - r) <= vg <= rnd(h + r):
+        # vg must be a code under this exponent and within the rounded range
+        if rnd(vg) != vg or not rnd(h - r) <= vg <= rnd(h + r):
             continue
         og = _e4m3_ordered(orc.e4m3_rne_sat(vg / sc))
         oh = _e4m3_ordered(orc.e4m3_rne_sat(h / sc))
@@ -328,15 +354,26 @@ def check_moe_values(orc, *, K, gran, act_mode, h_gpu, y_gpu, ref_y, ref_h,
 
 
 def read_h(fp4, packed, ws, T, k, I, tokens):
-    """The GPU's rounded h rows of `tokens` [ntok, k, I] from the workspace."""
+    """The GPU's rounded h rows of `tokens` [ntok, k, I] from the workspace
+    (bf16 values, or E4M3 bytes times their UE8M0 group scales)."""
     offs = fp4.moe_workspace_offsets(packed, T, k)
     P = T * k
     inv = ws[offs["inv"]:offs["inv"] + 4 * P].view(torch.int32).cpu().numpy()
-    hb = ws[offs["h"]:offs["h"] + 2 * P * I].view(torch.int16).view(
-        torch.bfloat16).view(P, I)
     rows = [int(inv[t * k + j]) for t in tokens for j in range(k)]
-    h = hb[torch.tensor(rows, device=hb.device)].float().cpu().numpy()
-    return h.astype(np.float64).reshape(len(tokens), k, I)
+    ridx = torch.tensor(rows, device=ws.device)
+    if offs["h_format"] == 0:
+        hb = ws[offs["h"]:offs["h"] + 2 * P * I].view(torch.int16).view(
+            torch.bfloat16).view(P, I)
+        h = hb[ridx].float().cpu().numpy().astype(np.float64)
+    else:
+        pitch = offs["pitch"]
+        h8 = ws[offs["h"]:offs["h"] + P * I].view(P, I)[ridx].cpu()
+        q = h8.view(torch.float8_e4m3fn).double().numpy()
+        hs = ws[offs["h_scales"]:offs["h_scales"] + (I // 128) * pitch * 4]
+        hs = hs.view(I // 128, pitch, 4).cpu().numpy()
+        sb = hs[:, rows, :].transpose(1, 0, 2).reshape(len(rows), I // 32)
+        h = q * np.repeat(np.ldexp(1.0, sb.astype(np.int64) - 127), 32, axis=-1)
+    return h.reshape(len(tokens), k, I)
 
 
 def check_moe(orc, fp4, cfg, packed, y, ws, tokens, ref_y, ref_h, ref_aux,

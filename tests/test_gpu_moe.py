@@ -8,7 +8,8 @@ import torch
 
 import block_scaled_fp4_02_gb300 as fp4
 import synth
-from _util import (bf16_tensor, check_moe, decode_packed, dequant_reference,
+from _util import (bf16_tensor, check_moe, decode_packed, decode_packed_mx,
+                   dequant_reference,
                    requant_weights_oracle, weights_for)
 
 pytestmark = pytest.mark.gpu
@@ -107,11 +108,20 @@ def test_prepare_layout_roundtrip(orc, gran, act, layout):
     assert d.gran_k == rg
     ref13 = dequant_reference(ref_w["w13"], ref_w["w13_s"], rg, ref_w["w13_gs"])
     ref2 = dequant_reference(ref_w["w2"], ref_w["w2_s"], rg, ref_w["w2_gs"])
-    got13 = decode_packed(bufs["w13"].numpy(), E, 2 * I, K, rg, d.scale_mul,
-                          d.scale_add, bufs["alpha13"].numpy(), True, I,
-                          layout)
-    got2 = decode_packed(bufs["w2"].numpy(), E, K, I, rg, d.scale_mul,
-                         d.scale_add, bufs["alpha2"].numpy(), False)
+    # FP8 activations over group32 weights: the block-scaled layout
+    assert d.layout == (1 if (act & 0xFF) == fp4.ACT_FP8 and rg == 32 else 0)
+    if d.layout == 1:
+        got13 = decode_packed_mx(bufs["w13"].numpy(),
+                                 bufs["w13_scales"].numpy(), E, 2 * I, K,
+                                 bufs["alpha13"].numpy(), True, I, layout)
+        got2 = decode_packed_mx(bufs["w2"].numpy(), bufs["w2_scales"].numpy(),
+                                E, K, I, bufs["alpha2"].numpy(), False)
+    else:
+        got13 = decode_packed(bufs["w13"].numpy(), E, 2 * I, K, rg,
+                              d.scale_mul, d.scale_add,
+                              bufs["alpha13"].numpy(), True, I, layout)
+        got2 = decode_packed(bufs["w2"].numpy(), E, K, I, rg, d.scale_mul,
+                             d.scale_add, bufs["alpha2"].numpy(), False)
     # Exact: every packed value equals e2m1 * scale * gs of the source.
     np.testing.assert_array_equal(got13, ref13)
     np.testing.assert_array_equal(got2, ref2)
