@@ -56,14 +56,18 @@ WORKLOADS = {"prefill": synth.PREFILL, "decode": synth.DECODE,
              "decode_t16": synth.MoeConfig(
                  "decode_w4a16_E256_K6144_I2048_T16_k8", 256, 6144, 2048, 16,
                  8, weight_seed=1003, input_seed=2116),
-             # small cases of the same kernels for ncu captures (inputs larger
-             # than L2, a few GB on the device at most)
+             # small cases of the same kernels for ncu captures: inputs larger
+             # than L2, a few GB on the device at most, and 19 experts so
+             # the GEMM work units are a multiple of the 152 SMs (no tail)
              "prefill_small": synth.MoeConfig(
-                 "prefill_small_w4a16_E16_K6144_I2048_T512_k8", 16, 6144, 2048,
-                 512, 8, weight_seed=1013, input_seed=2024),
+                 "prefill_small_w4a16_E19_K6144_I2048_T608_k8", 19, 6144, 2048,
+                 608, 8, weight_seed=1013, input_seed=2024),
              "decode_small": synth.MoeConfig(
-                 "decode_small_w4a16_E32_K6144_I2048_T8_k8", 32, 6144, 2048, 8,
-                 8, weight_seed=1023, input_seed=2034)}
+                 "decode_small_w4a16_E19_K6144_I2048_T8_k8", 19, 6144, 2048, 8,
+                 8, weight_seed=1023, input_seed=2035),
+             "fp8_small": synth.MoeConfig(
+                 "fp8_small_E19_K7168_I2048_T608_k8", 19, 7168, 2048, 608, 8,
+                 act="fp8", weight_seed=1015, input_seed=2025)}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 

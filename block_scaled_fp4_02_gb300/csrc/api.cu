@@ -233,13 +233,12 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   stage_mark(3, st);
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 
-  CUtensorMap m1[5], m2[5];
-  const uint32_t boxes[4] = {64, 128, 192, 256};
-  bool ok = make_e2m1_tmap(&m1[0], p->w13, static_cast<uint64_t>(p->E) * 2 * p->I, p->K) &&
-            make_e2m1_tmap(&m2[0], p->w2, static_cast<uint64_t>(p->E) * p->K, p->I);
-  for (int i = 0; i < 4 && ok; ++i)
-    ok = make_u8_tmap(&m1[1 + i], xperm, P, p->K, boxes[i]) &&
-         make_u8_tmap(&m2[1 + i], h8, P, p->I, boxes[i]);
+  MxMaps m1, m2;
+  bool ok = make_e2m1_tmap(&m1.w, p->w13, static_cast<uint64_t>(p->E) * 2 * p->I, p->K) &&
+            make_e2m1_tmap(&m2.w, p->w2, static_cast<uint64_t>(p->E) * p->K, p->I);
+  for (int i = 0; i < kMxBoxes && ok; ++i)
+    ok = make_u8_tmap(&m1.x[i], xperm, P, p->K, 32u * (i + 1)) &&
+         make_u8_tmap(&m2.x[i], h8, P, p->I, 32u * (i + 1));
   if (!ok) return FP4MOE_ERR_CUDA;
   MxGemmArgs a1{};
   a1.wscale = p->s13; a1.xscale = xs; a1.alpha = p->alpha; a1.offsets = offsets;

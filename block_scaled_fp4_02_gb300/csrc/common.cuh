@@ -315,6 +315,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
 
 // ------------------------------------------------------------ small math
 
+// Maximum of v over the 32 lanes of the warp (all lanes active).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t rotl32(uint32_t x, uint32_t r) {
   return __funnelshift_l(x, x, r);
 }

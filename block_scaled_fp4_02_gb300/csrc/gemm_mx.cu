@@ -28,7 +28,7 @@
 //   0      weight producer: TMA of the unit's weight tiles and bulk copy of
 //          their scale words, per step, into a ring of stages;
 //   1, 3   MMA issuers of tile 0 and tile 1 (one elected thread each);
-//   2      activation producer: TMA of the chunk's rows (boxes of 64..256
+//   2      activation producer: TMA of the chunk's rows (one box of 32..256
 //          rows) and bulk copy of their scale words;
 //   4..7   scale warps (TMEM lane quarters 0..3): scale words -> TMEM;
 //   8..15  epilogue (lane quarter = warp % 4; two warps per quarter).
@@ -43,7 +43,6 @@ namespace fp4moe {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kWarps = 16, kThreads = kWarps * 32;
 constexpr int kWarpA = 0, kWarpMma0 = 1, kWarpB = 2, kWarpMma1 = 3, kWarpSf0 = 4,
               kWarpEpi0 = 8, kEpiWarps = 8;
@@ -63,10 +62,15 @@ constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kOffB % 1024 == 0 && kStage % 1024 == 0, "swizzled operands need 1 KB alignment");
 static_assert(kOffSfa % 16 == 0 && kOffSfb % 16 == 0, "bulk copies need 16 B alignment");
-// TMEM: accumulators at columns 0 and 256 (N <= 224 each), scale slots of 16
-// columns from 480 (tile 0 SFA: +0..3, tile 1 SFA: +4..7, SFB: +8..15).
-constexpr uint32_t kAcc1Col = 256, kSfCol = 480, kTmemCols = 512;
-static_assert(kAcc1Col + kMxChunk <= kSfCol && kSfCol + 16 * kMxSfSlots <= kTmemCols,
+// TMEM: accumulators at columns 0 and 256 (N <= 224 each); four scale slots
+// of 16 columns in the two gaps, at 224, 240, 480 and 496 (tile 0 SFA:
+// +0..3, tile 1 SFA: +4..7, SFB: +8..15).
+constexpr uint32_t kAcc1Col = 256, kTmemCols = 512;
+__host__ __device__ constexpr uint32_t sf_col(int j) {
+  return j < 2 ? 224u + 16u * j : 480u + 16u * (j - 2);
+}
+static_assert(kMxChunk <= 224 && kAcc1Col + kMxChunk <= sf_col(2) &&
+              sf_col(1) + 16 <= kAcc1Col && sf_col(kMxSfSlots - 1) + 16 <= kTmemCols,
               "TMEM budget");
 static_assert(kMxChunk % 32 == 0 && (kMxChunk + 31) / 32 <= 8, "SFB columns");
 
@@ -100,11 +104,7 @@ __device__ __forceinline__ uint64_t desc_at(uint32_t saddr) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmW,
-                       const __grid_constant__ CUtensorMap tmX64,
-                       const __grid_constant__ CUtensorMap tmX128,
-                       const __grid_constant__ CUtensorMap tmX192,
-                       const __grid_constant__ CUtensorMap tmX256, const MxGemmArgs a) {
+    moe_gemm_mx_kernel(const __grid_constant__ MxMaps maps, const MxGemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -142,13 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done_bar, 2);
     fence_barrier_init();
   }
-  if (warp == kWarpA && lane == 0) prefetch_tensormap(&tmW);
-  if (warp == kWarpB && lane == 0) {
-    prefetch_tensormap(&tmX64);
-    prefetch_tensormap(&tmX128);
-    prefetch_tensormap(&tmX192);
-    prefetch_tensormap(&tmX256);
-  }
+  if (warp == kWarpA && lane == 0) prefetch_tensormap(&maps.w);
+  if (warp == kWarpB && lane < kMxBoxes) prefetch_tensormap(&maps.x[lane]);
   if (warp == kWarpMma0) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -171,9 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // FC1 rows of block b: gate tile at 256 b, up tile at 256 b + 128;
         // FC2 rows: tiles at 128 (2 nb) and 128 (2 nb + 1).
         const int wrow0 = U.e * a.rows_per_expert + 256 * U.nb;
-        const int brows = (U.ntok + 63) & ~63;        // box rows: 64 .. 256
-        const CUtensorMap* tmX = brows <= 64 ? &tmX64 : brows <= 128 ? &tmX128
-                               : brows <= 192 ? &tmX192 : &tmX256;
+        const int brows = (U.ntok + 31) & ~31;        // box rows: 32 .. 256
+        const CUtensorMap* tmX = &maps.x[brows / 32 - 1];
         const int lead = U.row0 & 3;                   // scale words before row0
         const uint32_t sfb_bytes = static_cast<uint32_t>(((lead + brows + 3) & ~3) * 4);
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
@@ -184,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (isA) {
             mbar_arrive_expect_tx(fullS(s), tiles * (kATileTx + kSfaBytes));
             for (int t = 0; t < tiles; ++t) {
-              tma_load_2d(st + kOffA + t * kATile, &tmW, ks * kMxK, wrow0 + 128 * t, fullS(s));
+              tma_load_2d(st + kOffA + t * kATile, &maps.w, ks * kMxK, wrow0 + 128 * t,
+                          fullS(s));
               // scale words of tile t at step ks: [tile group][ks][128 rows]
               const int64_t tg = static_cast<int64_t>(U.e) * a.tiles_per_expert + 2 * U.nb + t;
               bulk_load(st + kOffSfa + t * kSfaBytes,
@@ -231,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = sbase + s * kStage;
             const uint64_t ad = desc_at(st + kOffA + t * kATile);
             const uint64_t bd = desc_at(st + kOffB);
-            const uint32_t sfa = tmem + kSfCol + 16u * j + 4u * t;
-            const uint32_t sfb = tmem + kSfCol + 16u * j + 8u;
+            const uint32_t sfa = tmem + sf_col(j) + 4u * t;
+            const uint32_t sfb = tmem + sf_col(j) + 8u;
 #pragma unroll
             for (int kk = 0; kk < kMxK / 32; ++kk)
               umma_mx(d_tmem, ad + 2u * kk, bd + 2u * kk,
@@ -276,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* sfa = reinterpret_cast<const uint32_t*>(st + kOffSfa);
         const uint32_t* sfb = reinterpret_cast<const uint32_t*>(st + kOffSfb) + lead;
         const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t col = tmem + lanes + kSfCol + 16u * j;
+        const uint32_t col = tmem + lanes + sf_col(j);
         for (int t = 0; t < tiles; ++t) tmem_st1(col + 4u * t + q, sfa[t * 128 + 32 * q + lane]);
         uint32_t v[8];
 #pragma unroll
@@ -337,10 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gv = __uint_as_float(g[c]) * alpha;
             const float uv = __uint_as_float(up[c]) * alpha;
             const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-            float amax = fabsf(h);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-              amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+            // group maximum of |h| over the warp: non-negative floats order
+            // like their bit patterns
+            const float amax = __uint_as_float(redux_max_u32(__float_as_uint(fabsf(h))));
             const uint32_t byte = ue8m0_for_e4m3(amax);
             const float inv = pow2_any(127 - static_cast<int>(byte));
             const uint32_t code = f32x2_to_e4m3x2(h * inv, 0.0f) & 0xFFu;
@@ -373,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mx_mode(const CUtensorMap (&maps)[5], const MxGemmArgs& a, int grid,
+cudaError_t launch_mx_mode(const MxMaps& maps, const MxGemmArgs& a, int grid,
                            cudaStream_t st) {
   static std::mutex mu;
   static bool attr_set[kMaxDevices] = {};
@@ -391,14 +385,13 @@ cudaError_t launch_mx_mode(const CUtensorMap (&maps)[5], const MxGemmArgs& a, in
       attr_set[dev] = true;
     }
   }
-  moe_gemm_mx_kernel<MODE><<<grid, kThreads, kSmem, st>>>(maps[0], maps[1], maps[2], maps[3],
-                                                         maps[4], a);
+  moe_gemm_mx_kernel<MODE><<<grid, kThreads, kSmem, st>>>(maps, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_mx(const CUtensorMap (&maps)[5], const MxGemmArgs& a, int num_sms,
+cudaError_t launch_gemm_mx(const MxMaps& maps, const MxGemmArgs& a, int num_sms,
                            cudaStream_t st) {
   const int grid = num_sms > 0 ? num_sms : 1;
   if (a.mode == kGemmModeFc2) return launch_mx_mode<kGemmModeFc2>(maps, a, grid, st);

@@ -96,7 +96,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
 constexpr int kMxK = 128;             // K elements per step
 constexpr int kMxChunk = 224;         // tokens per unit (accumulator columns)
 constexpr int kMxChunk256Rows = 256;  // largest activation box (rows)
-constexpr int kMxSfSlots = 2;         // scale-factor slots in TMEM
+constexpr int kMxSfSlots = 4;         // scale-factor slots in TMEM
 struct MxGemmArgs {
   const uint32_t* wscale;  // [E][tiles][ksteps][128] UE8M0 words (4 blocks)
   const uint32_t* xscale;  // [ksteps][xscale_pitch] words of the B rows
@@ -124,10 +124,16 @@ cudaError_t launch_mx_scales(const uint8_t* s, int E, int N, int Kd, bool gated,
 cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
                              const uint8_t* xs, int K, int64_t pitch, uint8_t* xperm,
                              uint32_t* xsperm, cudaStream_t st);
-// maps: weights (16U4_ALIGN16B, 128 x 128 boxes), then the activation rows
-// with boxes of 64, 128, 192 and 256 rows (E4M3, 128-byte swizzle).
-cudaError_t launch_gemm_mx(const CUtensorMap (&maps)[5], const MxGemmArgs& a,
-                           int num_sms, cudaStream_t st);
+// Tensor maps of one block-scaled GEMM: the weights (16U4_ALIGN16B, 128 x
+// 128 boxes) and the activation rows with boxes of 32, 64, ..., 256 rows
+// (E4M3, 128-byte swizzle).
+constexpr int kMxBoxes = 8;
+struct MxMaps {
+  CUtensorMap w;
+  CUtensorMap x[kMxBoxes];   // x[j]: boxes of 32 (j + 1) rows
+};
+cudaError_t launch_gemm_mx(const MxMaps& maps, const MxGemmArgs& a, int num_sms,
+                           cudaStream_t st);
 
 // Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
 int gemm_chunk_max(int T);
