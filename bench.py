@@ -199,8 +199,9 @@ class MoeRun:
         self.touched = int((r["counts"] > 0).sum().item())
         torch.cuda.synchronize()
         d = self.packed.desc
-        self.w13_bytes_per_expert = d.w13_bytes // cfg.E
-        self.w2_bytes_per_expert = d.w2_bytes // cfg.E
+        self.mx = d.layout == 1          # block-scaled path (FP8 x group32)
+        self.w13_bytes_per_expert = (d.w13_bytes + d.w13_scales_bytes) // cfg.E
+        self.w2_bytes_per_expert = (d.w2_bytes + d.w2_scales_bytes) // cfg.E
 
     def step(self):
         fp4 = self.fp4
@@ -290,21 +291,28 @@ class MoeRun:
         return self.touched * (self.w13_bytes_per_expert +
                                self.w2_bytes_per_expert)
 
+    def _act_bytes(self, n: int) -> float:
+        """Bytes of one gathered activation (or h) row of n elements: bf16,
+        FP32 h on the kept-group16 FP8 path, E4M3 + one UE8M0 byte per 32 on
+        the block-scaled path."""
+        return n * (1 + 1 / 32) if self.mx else n * 2
+
     def fc1_bytes(self) -> int:
         """Algorithmic FC1 bytes: touched experts' packed FC1 weights, the
         gathered activations read once and h written once."""
         c = self.cfg
         P = c.T * c.top_k
-        return (self.touched * self.w13_bytes_per_expert + P * c.K * 2 +
-                P * c.I * (4 if self.fp8 else 2))
+        h = P * c.I * 4 if (self.fp8 and not self.mx) else P * self._act_bytes(c.I)
+        return int(self.touched * self.w13_bytes_per_expert +
+                   P * self._act_bytes(c.K) + h)
 
     def fc2_bytes(self) -> int:
         """Algorithmic FC2 bytes: touched experts' packed FC2 weights, h read
         once and the FP32 FC2 output written once."""
         c = self.cfg
         P = c.T * c.top_k
-        return (self.touched * self.w2_bytes_per_expert + P * c.I * 2 +
-                P * c.K * 4)
+        return int(self.touched * self.w2_bytes_per_expert +
+                   P * self._act_bytes(c.I) + P * c.K * 4)
 
     def free(self):
         self.packed.free()
