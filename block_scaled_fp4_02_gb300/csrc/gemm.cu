@@ -17,8 +17,8 @@
 //     issue is spread and amortized: the unit of hand-off is a pair of K
 //     steps (128 wide: one weight copy, one TMEM A stage of 64 columns, eight
 //     MMAs); four MMA warps take pairs m = 0..3 (mod 4) into their own
-//     accumulators (summed in the epilogue, double-buffered), and four
-//     threads load the activation rows (steps n = 0..3 (mod 4)).
+//     accumulators (summed in the epilogue), and four threads load the
+//     activation rows (steps n = 0..3 (mod 4)).
 // Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
 //                 (MT per K step, or two K steps with NT = 32) into a ring of
@@ -33,7 +33,8 @@
 //   warps 3..18 : dequantizers: NT = 256, two groups of eight (warp w owns
 //                 rows 32*(w%4).. and one 32-wide K half; group g fills
 //                 weight tile g of every step); NT = 32, four groups of four
-//                 (group g converts the pairs m = g (mod 4) into A stage g);
+//                 (group g converts the pairs m = g (mod 4) into A stage
+//                 m mod 6);
 //   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
 //                 reading the TMEM accumulators; then NT = 256 has the MMA
 //                 warp of tile 1, NT = 32 its four MMA warps (one per SM
@@ -85,16 +86,21 @@ struct Cfg {
   // an F stage and an A stage hold a pair of K steps, a B stage one step.
   static constexpr int kStepsPerF = kATmem ? 2 : 1;  // K steps per F stage
   static constexpr int kSF = kATmem ? 12 : 6;
-  static constexpr int kSAa = kATmem ? 4 : 2;      // TMEM A: 4 x 64 columns (two K tiles)
-  static constexpr int kSB = kATmem ? 8 : 3;
+  // TMEM A: six stages of 64 columns (a pair of K tiles each), shared round
+  // robin by the four dequant groups, so a group converts its next pair while
+  // the MMAs of its previous one are still in flight.
+  static constexpr int kSAa = kATmem ? 6 : 2;
+  static constexpr int kSB = kATmem ? 2 * kSAa : 3;
   static constexpr uint32_t kFStage = kFBytes * kMT * kStepsPerF;
   static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
   static constexpr uint32_t kBStage = NT * 128;    // NT rows x 64 bf16
   // Activation rows per TMA box (the tensor map is built to match): boxes
   // of 64 rows cut the copies per step four-fold for many-token chunks.
   static constexpr int kBoxRows = kATmem ? 16 : 64;
-  static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
-  static constexpr int kAccBufs = kATmem ? 2 : 1;
+  // TMEM A: the four MMA warps' accumulators (single-buffered: the decode
+  // epilogue drains in a few hundred cycles) in columns 0..127, A from 128.
+  static constexpr uint32_t kATmemCol = 128;       // first TMEM column of A
+  static constexpr int kAccBufs = 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
   // Dequant warps per stage: TMEM A splits the 16 warps into four groups of
   // four (one row quarter and a whole pair of K steps each), NT=256 into
@@ -114,7 +120,7 @@ struct Cfg {
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
                           kATmemCol + 64 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
-  static_assert(!kATmem || (kSB == 2 * kSAa && kSF % 4 == 0 && kSAa == 4),
+  static_assert(!kATmem || kSB == 2 * kSAa,
                 "TMEM A rings: B stages released with their pair's A stage");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
@@ -391,16 +397,18 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
-    const uint32_t t_st = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
-                          static_cast<uint32_t>(grp) * 64u;
-    int sf = grp;
-    uint32_t phf = 0, pha = 0;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol;
     uint32_t n = 0;                   // K steps of this CTA before the unit
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       for (int ks = 2 * ((grp - static_cast<int>(n >> 1)) & 3); ks < a.ksteps; ks += 8) {
+        // CTA-wide pair index: weight stage m % SF, A stage m % SAa.
+        const uint32_t m = (n + static_cast<uint32_t>(ks)) >> 1;
+        const int sf = static_cast<int>(m % SF), sa = static_cast<int>(m % SAa);
+        const uint32_t phf = (m / SF) & 1u, pha = (m / SAa) & 1u;
+        const uint32_t t_st = t_row + static_cast<uint32_t>(sa) * 64u;
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
+        if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
         tc_fence_after();             // after the MMA that last read this stage
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -439,10 +447,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aready(grp));
-        sf += 4;
-        if (sf >= SF) { sf -= SF; phf ^= 1u; }
-        pha ^= 1u;
+        if (lane == 0) mbar_arrive(aready(sa));
       }
       n += static_cast<uint32_t>(a.ksteps);
     }

@@ -31,7 +31,9 @@
 //   2      activation producer: TMA of the chunk's rows (one box of 32..256
 //          rows) and bulk copy of their scale words;
 //   4..7   scale warps (TMEM lane quarters 0..3): scale words -> TMEM;
-//   8..15  epilogue (lane quarter = warp % 4; two warps per quarter).
+//   8..23  epilogue (lane quarter = warp % 4; four warps per quarter share
+//          the accumulator columns, so the single-buffered accumulators drain
+//          quickly between units).
 // All waits are bounded (about 2 s); a timeout records FP4MOE_ERR_TIMEOUT in
 // the device status word and the CTA winds down and frees its TMEM.
 #include <mutex>
@@ -43,9 +45,9 @@ namespace fp4moe {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kWarps = 16, kThreads = kWarps * 32;
+constexpr int kWarps = 24, kThreads = kWarps * 32;
 constexpr int kWarpA = 0, kWarpMma0 = 1, kWarpB = 2, kWarpMma1 = 3, kWarpSf0 = 4,
-              kWarpEpi0 = 8, kEpiWarps = 8;
+              kWarpEpi0 = 8, kEpiWarps = 16;
 constexpr int kStages = 3;
 constexpr uint32_t kATile = 128 * 128;             // 128 rows x 128 B (widened E2M1)
 constexpr uint32_t kATileTx = 128 * 64;            // bytes the TMA reads (packed)
@@ -286,9 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
   } else {
     // --------------------------------------------------------- epilogue
-    const int ew = warp - kWarpEpi0;   // 0..7
+    const int ew = warp - kWarpEpi0;   // 0..15
     const int q = warp & 3;            // TMEM lane quarter
-    const int half = ew >> 2;          // FC1: column half; FC2: tile
+    const int part = ew >> 2;          // 0..3: FC1 column part; FC2 tile + half
+    const int tile = part & 1;         // FC2: the accumulator (weight tile) it drains
     const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
     uint32_t acc_ph = 0;
     bool ok = true;
@@ -299,12 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = __ldg(a.alpha + U.e);
       const int nchunks = (U.ntok + 15) >> 4;
       if (MODE == kGemmModeFc2) {
-        const int nb = 2 * U.nb + half;
+        const int nb = 2 * U.nb + tile;
         if (nb < a.nblocks) {
           float* o = static_cast<float*>(a.out);
           const int64_t col_n = static_cast<int64_t>(nb) * 128 + 32 * q + lane;
-          const uint32_t tb = tmem + lanes + (half ? kAcc1Col : 0u);
-          for (int c0 = 0; c0 < nchunks; ++c0) {
+          const uint32_t tb = tmem + lanes + (tile ? kAcc1Col : 0u);
+          for (int c0 = part >> 1; c0 < nchunks; c0 += 2) {
             uint32_t v[16];
             tmem_ld16(tb + 16 * c0, v);
             tmem_ld_wait();
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // h for i = 128 b + 32 q + lane; the 32 lanes are one (1,1,32) group.
         uint8_t* h8 = static_cast<uint8_t*>(a.out);
         const int64_t i = static_cast<int64_t>(U.nb) * 128 + 32 * q + lane;
-        for (int c0 = half; c0 < nchunks; c0 += 2) {
+        for (int c0 = part; c0 < nchunks; c0 += 4) {
           uint32_t g[16], up[16];
           tmem_ld16(tmem + lanes + 16 * c0, g);
           tmem_ld16(tmem + lanes + kAcc1Col + 16 * c0, up);
