@@ -35,8 +35,9 @@
 //                 weight tile g of every step); NT = 32, four groups of four
 //                 (group g converts the pairs m = g (mod 4) into A stage
 //                 m mod 6);
-//   warps 19..  : epilogue (eight warps for NT = 256, four for NT = 32),
-//                 reading the TMEM accumulators; then NT = 256 has the MMA
+//   warps 19..  : epilogue (twelve warps for NT = 256, three per lane
+//                 quarter; four for NT = 32), reading the TMEM accumulators;
+//                 then NT = 256 has the MMA
 //                 warp of tile 1, NT = 32 its four MMA warps (one per SM
 //                 sub-partition) and the activation producers of steps
 //                 n = 2, 3 (mod 4).
@@ -72,7 +73,10 @@ struct Cfg {
   // and split the pairs of K steps; with A in shared memory two MMA warps
   // each own one weight tile (all K steps).
   static constexpr int kMmaWarps = kATmem ? 4 : 2;
-  static constexpr int kEpiWarps = kATmem ? 4 : 8;
+  // Epilogue: NT = 32, one warp per TMEM lane quarter; NT = 256, three per
+  // quarter, which take the (tile, pair of chunks) items round robin so the
+  // single-buffered accumulators drain quickly between units.
+  static constexpr int kEpiWarps = kATmem ? 4 : 12;
   // The warps after the epilogue: TMEM A, the four MMA warps and then two
   // activation producers; shared-memory A, the MMA warp of tile 1 (warp 1
   // issues tile 0).
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int ew = warp - kWarpEpi0;  // 0 .. kEpiWarps-1
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     constexpr int kParts = C::kEpiWarps / 4;
-    const int part = ew >> 2;         // MT = 2: weight tile; MT = 1: column slice
+    const int part = ew >> 2;         // this warp's share of the quarter's work
     const int r = 32 * q + lane;      // weight row in the tile
     int buf = 0;
     uint32_t acc_ph = 0;
@@ -539,13 +543,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
       const int nchunks = (U.ntok + 15) >> 4;
-      const int nb = U.nb + (MT > 1 ? part : 0);
-      const bool live = nb < a.nblocks;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                              static_cast<uint32_t>(buf) * C::kAccCols +
-                              (MT > 1 ? 256u * part : 0u);
-      // Stores one 16-column chunk j of accumulator values v.
-      auto emit16 = [&](const uint32_t (&v)[16], int j) {
+                              static_cast<uint32_t>(buf) * C::kAccCols;
+      // Stores one 16-column chunk j of accumulator values v of weight
+      // block nb.
+      auto emit16 = [&](const uint32_t (&v)[16], int j, int nb) {
         if (MODE == kGemmModeFc2) {
           float* o = static_cast<float*>(a.out);
           const int64_t col_n = static_cast<int64_t>(nb) * kTileN + r;
@@ -582,19 +584,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
       };
       if (MT > 1) {
-        // All chunks of this warp's tile: two chunks (32 columns) per TMEM
-        // load and wait.
-        for (int j = 0; live && j < nchunks; j += 2) {
+        // Items (tile, pair of chunks), tiles interleaved, taken round robin
+        // by the kParts warps of this lane quarter; one TMEM load and wait
+        // per item (32 columns).
+        const int npairs = (nchunks + 1) >> 1;
+        for (int it = part; it < 2 * npairs; it += kParts) {
+          const int tile = it & 1, j = 2 * (it >> 1);
+          const int nb = U.nb + tile;
+          if (nb >= a.nblocks) continue;   // odd block count: no second tile
           uint32_t v[32];
-          tmem_ld32(t_base + 16 * j, v);
-          tmem_ld_wait();
+          tmem_ld32(t_base + 256u * tile + 16 * j, v);
+          tmem_ld_wait(v);
           uint32_t v0[16], v1[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) { v0[x] = v[x]; v1[x] = v[16 + x]; }
-          emit16(v0, j);
-          if (j + 1 < nchunks) emit16(v1, j + 1);
+          emit16(v0, j, nb);
+          if (j + 1 < nchunks) emit16(v1, j + 1, nb);
         }
       } else {
+        const int nb = U.nb;
+        const bool live = nb < a.nblocks;
         // Sum the partial accumulators (NT columns apart) of the MMA warps
         // that had K steps in this unit: warp m took the steps with
         // (n_unit + ks) % kMmaWarps == m, none when ksteps is short.
@@ -603,17 +612,17 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         for (int j = part; live && j < nchunks; j += kParts) {
           uint32_t v[16];
           tmem_ld16(t_base + static_cast<uint32_t>(m0 * NT) + 16 * j, v);
-          tmem_ld_wait();
+          tmem_ld_wait(v);
           for (int p = 1; p < nparts; ++p) {
             const int m = (m0 + p) % C::kMmaWarps;
             uint32_t w[16];
             tmem_ld16(t_base + static_cast<uint32_t>(m * NT) + 16 * j, w);
-            tmem_ld_wait();
+            tmem_ld_wait(w);
 #pragma unroll
             for (int x = 0; x < 16; ++x)
               v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
           }
-          emit16(v, j);
+          emit16(v, j, nb);
         }
       }
       tc_fence_before();

@@ -45,6 +45,7 @@ namespace fp4moe {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kWarps = 24, kThreads = kWarps * 32;
 constexpr int kWarpA = 0, kWarpMma0 = 1, kWarpB = 2, kWarpMma1 = 3, kWarpSf0 = 4,
               kWarpEpi0 = 8, kEpiWarps = 16;
@@ -307,12 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* o = static_cast<float*>(a.out);
           const int64_t col_n = static_cast<int64_t>(nb) * 128 + 32 * q + lane;
           const uint32_t tb = tmem + lanes + (tile ? kAcc1Col : 0u);
-          for (int c0 = part >> 1; c0 < nchunks; c0 += 2) {
-            uint32_t v[16];
-            tmem_ld16(tb + 16 * c0, v);
-            tmem_ld_wait();
+          // Pairs of chunks (32 columns) per TMEM load; the two warps of a
+          // tile and lane quarter take alternate pairs.
+          for (int c0 = 2 * (part >> 1); c0 < nchunks; c0 += 4) {
+            uint32_t v[32];
+            tmem_ld32(tb + 16 * c0, v);
+            tmem_ld_wait(v);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 32; ++c) {
               const int col = 16 * c0 + c;
               if (col < U.ntok)
                 o[static_cast<int64_t>(U.row0 + col) * a.ldo + col_n] =
@@ -322,33 +325,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // h for i = 128 b + 32 q + lane; the 32 lanes are one (1,1,32) group.
+        // Per chunk of 16 tokens each lane packs its 16 codes four per word;
+        // a transpose over the warp then gives lane L the codes of token
+        // 4k + L/8 for i = 4 (L % 8) .. + 3, stored as one 32-bit word, and
+        // lanes 0..15 store the 16 tokens' scale bytes at once.
         uint8_t* h8 = static_cast<uint8_t*>(a.out);
-        const int64_t i = static_cast<int64_t>(U.nb) * 128 + 32 * q + lane;
+        const int tr = lane >> 3, tm = lane & 7;
+        const int64_t i4 = static_cast<int64_t>(U.nb) * 128 + 32 * q + 4 * tm;
+        const uint32_t sel = static_cast<uint32_t>(tr) | (static_cast<uint32_t>(tr + 4) << 4);
         for (int c0 = part; c0 < nchunks; c0 += 4) {
           uint32_t g[16], up[16];
           tmem_ld16(tmem + lanes + 16 * c0, g);
           tmem_ld16(tmem + lanes + kAcc1Col + 16 * c0, up);
-          tmem_ld_wait();
+          tmem_ld_wait(g);
+          tmem_ld_wait(up);
+          uint32_t packed[4] = {0u, 0u, 0u, 0u};
+          uint32_t my_sb = 0u;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const int col = 16 * c0 + c;
             const float gv = __uint_as_float(g[c]) * alpha;
             const float uv = __uint_as_float(up[c]) * alpha;
             const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             // group maximum of |h| over the warp: non-negative floats order
             // like their bit patterns
             const float amax = __uint_as_float(redux_max_u32(__float_as_uint(fabsf(h))));
-            const uint32_t byte = ue8m0_for_e4m3(amax);
-            const float inv = pow2_any(127 - static_cast<int>(byte));
+            const uint32_t byte = ue8m0_for_e4m3(amax);   // <= 247 for finite h
+            const float inv = __uint_as_float((254u - byte) << 23);   // 2^(127 - byte)
             const uint32_t code = f32x2_to_e4m3x2(h * inv, 0.0f) & 0xFFu;
-            if (col < U.ntok) {
-              const int64_t row = U.row0 + col;
-              h8[row * a.ldo + i] = static_cast<uint8_t>(code);
-              if (lane == 0)
-                a.hscale[(static_cast<int64_t>(U.nb) * a.hscale_pitch + row) * 4 + q] =
-                    static_cast<uint8_t>(byte);
-            }
+            packed[c >> 2] |= code << (8 * (c & 3));
+            if (lane == c) my_sb = byte;
           }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t b0 = __shfl_sync(kFullMask, packed[k], 4 * tm + 0);
+            const uint32_t b1 = __shfl_sync(kFullMask, packed[k], 4 * tm + 1);
+            const uint32_t b2 = __shfl_sync(kFullMask, packed[k], 4 * tm + 2);
+            const uint32_t b3 = __shfl_sync(kFullMask, packed[k], 4 * tm + 3);
+            const uint32_t w = __byte_perm(__byte_perm(b0, b1, sel), __byte_perm(b2, b3, sel),
+                                           0x5410);
+            const int col = 16 * c0 + 4 * k + tr;
+            if (col < U.ntok)
+              *reinterpret_cast<uint32_t*>(h8 + static_cast<int64_t>(U.row0 + col) * a.ldo + i4) = w;
+          }
+          if (lane < 16 && 16 * c0 + lane < U.ntok)
+            a.hscale[(static_cast<int64_t>(U.nb) * a.hscale_pitch + U.row0 + 16 * c0 + lane) * 4 +
+                     q] = static_cast<uint8_t>(my_sb);
         }
       }
       tc_fence_before();
