@@ -5,6 +5,11 @@ loads the in-tree shared library, turns torch tensors into device pointers and
 the current CUDA stream, and raises on a non-zero status.  There is no CPU or
 PyTorch fallback: if the library is missing or was not built, every call fails
 loudly (``build()`` compiles it).
+
+With the environment variable FP4MOE_BOUNDS_CHECK=1 set before the first
+call, the bounds-checked variant of the library (libfp4moe_checked.so, same
+sources, every data-dependent index checked on the device; a failed check
+records ERR_BOUNDS) is loaded instead.
 """
 from __future__ import annotations
 
@@ -24,11 +29,12 @@ __all__ = [
     "prepare_weights", "PackedWeights", "moe_workspace_size", "moe_forward",
     "moe_workspace_size_host", "moe_forward_host", "status_string",
     "last_device_error", "set_stage_events", "STAGE_NAMES",
-    "test_wait_timeout",
+    "test_wait_timeout", "test_bounds_check", "build_flags", "variant",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, \
-    ERR_TIMEOUT = range(6)
+    ERR_TIMEOUT, ERR_BOUNDS = range(7)
+BUILD_BOUNDS_CHECK = 1
 W13_GATE_UP, W13_UP_GATE = 0, 1
 ACT_BF16, ACT_FP8 = 0, 1
 FLAG_NO_REQUANT = 0x100
@@ -63,9 +69,17 @@ class PackedDesc(ctypes.Structure):
     ]
 
 
-def build(force: bool = False) -> str:
-    """Compile the CUDA library for sm_103a (in-tree)."""
-    return _build.build(force=force)
+def variant() -> str:
+    """Library variant this process loads: "checked" when FP4MOE_BOUNDS_CHECK
+    is set to a non-empty value other than 0, else "release"."""
+    v = os.environ.get("FP4MOE_BOUNDS_CHECK", "")
+    return "checked" if v not in ("", "0") else "release"
+
+
+def build(force: bool = False, variant_name: str | None = None) -> str:
+    """Compile the CUDA library for sm_103a (in-tree): the variant this
+    process loads unless one is named."""
+    return _build.build(force=force, variant=variant_name or variant())
 
 
 def exported_symbols() -> list[str]:
@@ -80,11 +94,12 @@ def load() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(_build.LIB):
+        path = _build.lib_path(variant())
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{_build.LIB} is missing: build it with "
+                f"{path} is missing: build it with "
                 "block_scaled_fp4_02_gb300.build() (needs nvcc)")
-        L = ctypes.CDLL(_build.LIB)
+        L = ctypes.CDLL(path)
         vp, sz, i32, i64 = (ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                             ctypes.c_int64)
         sigs = {
@@ -111,6 +126,8 @@ def load() -> ctypes.CDLL:
             "fp4moe_moe_workspace_offsets": (i32, [vp, i32, i32,
                                                    ctypes.POINTER(sz), i32]),
             "fp4moe_test_wait_timeout": (i32, [ctypes.c_uint64, vp]),
+            "fp4moe_test_bounds_check": (i32, [i64, vp]),
+            "fp4moe_build_flags": (i32, []),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -126,7 +143,9 @@ def status_string(code: int) -> str:
     except Exception:  # library not loadable: still give a message
         return {0: "ok", 1: "invalid argument", 2: "unsupported",
                 3: "workspace too small", 4: "CUDA error",
-                5: "device wait timed out"}.get(code, "unknown status")
+                5: "device wait timed out",
+                6: "index out of bounds (bounds-checked build)"}.get(
+                    code, "unknown status")
 
 
 def _check(code: int, what: str) -> None:
@@ -182,6 +201,19 @@ def test_wait_timeout(limit_ns: int, stream=None) -> None:
     status word (read it with last_device_error())."""
     _check(load().fp4moe_test_wait_timeout(limit_ns, _stream(stream)),
            "test_wait_timeout")
+
+
+def test_bounds_check(index: int, stream=None) -> None:
+    """Launches the index-check self-test: slot `index` of a 64-entry device
+    array is written through the check of the bounds-checked build; outside
+    [0, 64) it records ERR_BOUNDS (read it with last_device_error())."""
+    _check(load().fp4moe_test_bounds_check(index, _stream(stream)),
+           "test_bounds_check")
+
+
+def build_flags() -> int:
+    """BUILD_BOUNDS_CHECK if the loaded library is the bounds-checked one."""
+    return int(load().fp4moe_build_flags())
 
 
 # ------------------------------------------------------------------- steps

@@ -226,10 +226,10 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   stage_mark(2, st);
   if (e == cudaSuccess)
     e = launch_scatter(ids, T, p->E, top_k, base, perm, inv, nullptr, nullptr, 0,
-                       FP4MOE_ACT_FP8, nullptr, st);
+                       FP4MOE_ACT_FP8, nullptr, err, st);
   if (e == cudaSuccess)
     e = launch_gather_mx(inv, T, top_k, static_cast<const uint8_t*>(x), x_scales, p->K,
-                         L.pitch, xperm, xs, st);
+                         L.pitch, xperm, xs, err, st);
   stage_mark(3, st);
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 
@@ -243,6 +243,7 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   MxGemmArgs a1{};
   a1.wscale = p->s13; a1.xscale = xs; a1.alpha = p->alpha; a1.offsets = offsets;
   a1.cstart = cstart; a1.out = h8; a1.hscale = reinterpret_cast<uint8_t*>(hs); a1.err = err;
+  a1.rows = P;
   a1.E = p->E; a1.nblocks = p->I / 128; a1.ksteps = p->K / kMxK;
   a1.rows_per_expert = 2 * p->I; a1.tiles_per_expert = 2 * p->I / 128;
   a1.xscale_pitch = L.pitch; a1.hscale_pitch = L.pitch; a1.ldo = p->I;
@@ -258,7 +259,7 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   if (e == cudaSuccess) e = launch_gemm_mx(m2, a2, sms, st);
   stage_mark(6, st);
   if (e == cudaSuccess)
-    e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), st);
+    e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), err, st);
   stage_mark(7, st);
   return cuda_status(e);
 }
@@ -275,6 +276,7 @@ const char* fp4moe_status_string(int s) {
     case FP4MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case FP4MOE_ERR_CUDA: return "CUDA error";
     case FP4MOE_ERR_TIMEOUT: return "device wait timed out";
+    case FP4MOE_ERR_BOUNDS: return "index out of bounds (bounds-checked build)";
     default: return "unknown status";
   }
 }
@@ -361,7 +363,7 @@ int fp4moe_route_debug(const float* logits, int T, int E, int top_k,
     e = launch_scan(T, E, hist, base, counts, offsets, cstart, gemm_chunk_max(T), st);
   if (e == cudaSuccess)
     e = launch_scatter(ids, T, E, top_k, base, perm, inv, nullptr, nullptr, 0,
-                       FP4MOE_ACT_BF16, nullptr, st);
+                       FP4MOE_ACT_BF16, nullptr, status_word(), st);
   return cuda_status(e);
 }
 
@@ -586,7 +588,7 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   stage_mark(2, st);
   if (e == cudaSuccess)
     e = launch_scatter(ids, T, p->E, top_k, base, perm, inv, x, x_scales, p->K,
-                       p->act_mode, xperm, st);
+                       p->act_mode, xperm, err, st);
   stage_mark(3, st);
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 
@@ -597,7 +599,8 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
     return FP4MOE_ERR_CUDA;
   GemmArgs a1{};
   a1.wpack = p->w13; a1.alpha = p->alpha; a1.offsets = offsets; a1.cstart = cstart;
-  a1.err = err; a1.E = p->E; a1.nblocks = 2 * p->I / kTileN; a1.ksteps = p->K / kTileK;
+  a1.err = err; a1.rows = P; a1.E = p->E; a1.nblocks = 2 * p->I / kTileN;
+  a1.ksteps = p->K / kTileK;
   a1.tile_bytes = tile_bytes(p->gran); a1.gran = p->gran; a1.smul = p->smul;
   a1.sadd = p->sadd; a1.ldo = p->I;
   if (p->act_mode == FP4MOE_ACT_BF16) {
@@ -618,7 +621,7 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   if (e == cudaSuccess) e = launch_gemm(tm_h, a2, chunk, sms, st);
   stage_mark(6, st);
   if (e == cudaSuccess)
-    e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), st);
+    e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), err, st);
   stage_mark(7, st);
   return cuda_status(e);
 }

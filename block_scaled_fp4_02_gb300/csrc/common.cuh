@@ -18,6 +18,24 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Index checks.  The bounds-checked build (FP4MOE_BOUNDS_CHECK) tests every
+// data-dependent index against its buffer before the access; a failed check
+// records BOUNDS and the caller skips the access.  The release build compiles
+// the checks out (they always pass).  in_bounds<true> checks in both builds.
+#ifdef FP4MOE_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+template <bool kOn = kBoundsCheck>
+__device__ __forceinline__ bool in_bounds(int* err, int64_t i, int64_t n) {
+  if (!kOn) return true;
+  if (i >= 0 && i < n) return true;
+  record_error(err, FP4MOE_ERR_BOUNDS);
+  return false;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

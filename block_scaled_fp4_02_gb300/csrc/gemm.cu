@@ -17,8 +17,8 @@
 //     issue is spread and amortized: the unit of hand-off is a pair of K
 //     steps (128 wide: one weight copy, one TMEM A stage of 64 columns, eight
 //     MMAs); four MMA warps take pairs m = 0..3 (mod 4) into their own
-//     accumulators (summed in the epilogue), and four threads load the
-//     activation rows (steps n = 0..3 (mod 4)).
+//     accumulators (summed in the epilogue, double-buffered), and four
+//     threads load the activation rows (steps n = 0..3 (mod 4)).
 // Warp roles, one CTA per SM, persistent over units:
 //   warp 0      : weight producer -- bulk copies of the packed FP4 tiles
 //                 (MT per K step, or two K steps with NT = 32) into a ring of
@@ -33,8 +33,7 @@
 //   warps 3..18 : dequantizers: NT = 256, two groups of eight (warp w owns
 //                 rows 32*(w%4).. and one 32-wide K half; group g fills
 //                 weight tile g of every step); NT = 32, four groups of four
-//                 (group g converts the pairs m = g (mod 4) into A stage
-//                 m mod 6);
+//                 (group g converts the pairs m = g (mod 4) into A stage g);
 //   warps 19..  : epilogue (twelve warps for NT = 256, three per lane
 //                 quarter; four for NT = 32), reading the TMEM accumulators;
 //                 then NT = 256 has the MMA
@@ -90,10 +89,11 @@ struct Cfg {
   // an F stage and an A stage hold a pair of K steps, a B stage one step.
   static constexpr int kStepsPerF = kATmem ? 2 : 1;  // K steps per F stage
   static constexpr int kSF = kATmem ? 12 : 6;
-  // TMEM A: six stages of 64 columns (a pair of K tiles each), shared round
-  // robin by the four dequant groups, so a group converts its next pair while
-  // the MMAs of its previous one are still in flight.
-  static constexpr int kSAa = kATmem ? 6 : 2;
+  // TMEM A: four stages of 64 columns (a pair of K tiles each), stage g
+  // owned by dequant group g and by MMA warp g: every waiter on a stage's
+  // barriers sees each of its phases in turn (a waiter that skipped a phase
+  // could mistake an old phase for the one it waits for).
+  static constexpr int kSAa = kATmem ? 4 : 2;
   static constexpr int kSB = kATmem ? 2 * kSAa : 3;
   static constexpr uint32_t kFStage = kFBytes * kMT * kStepsPerF;
   static constexpr uint32_t kAStage = kATmem ? 0 : kABytes * kMT;
@@ -101,10 +101,10 @@ struct Cfg {
   // Activation rows per TMA box (the tensor map is built to match): boxes
   // of 64 rows cut the copies per step four-fold for many-token chunks.
   static constexpr int kBoxRows = kATmem ? 16 : 64;
-  // TMEM A: the four MMA warps' accumulators (single-buffered: the decode
-  // epilogue drains in a few hundred cycles) in columns 0..127, A from 128.
-  static constexpr uint32_t kATmemCol = 128;       // first TMEM column of A
-  static constexpr int kAccBufs = 1;
+  // TMEM A: the four MMA warps' double-buffered accumulators in columns
+  // 0..255, A from 256.
+  static constexpr uint32_t kATmemCol = 256;       // first TMEM column of A
+  static constexpr int kAccBufs = kATmem ? 2 : 1;
   static constexpr uint32_t kAccCols = kATmem ? NT * kMmaWarps : 512;  // per buffer
   // Dequant warps per stage: TMEM A splits the 16 warps into four groups of
   // four (one row quarter and a whole pair of K steps each), NT=256 into
@@ -124,8 +124,9 @@ struct Cfg {
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
                           kATmemCol + 64 * kSAa <= kTmemCols)
                        : kAccCols <= kTmemCols, "TMEM budget");
-  static_assert(!kATmem || kSB == 2 * kSAa,
-                "TMEM A rings: B stages released with their pair's A stage");
+  static_assert(!kATmem || (kSB == 2 * kSAa && kSF % 4 == 0 && kSAa == 4 && kMmaWarps == 4),
+                "TMEM A rings: stage g belongs to dequant group g and MMA warp g; "
+                "B stages released with their pair's A stage");
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
 };
@@ -138,14 +139,16 @@ struct Unit {
 // nbu * (cstart[e+1] - cstart[e]) consecutive units, nbu = ceil(nblocks/MT).
 // cs_/os are the shared-memory copies of cstart and offsets.
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
-                                            int mt, const int* cs_,
+                                            int mt, int max_tok, const int* cs_,
                                             const int* os, int u) {
   int lo = 0, hi = a.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (nbu * cs_[mid] <= u) lo = mid; else hi = mid;
   }
-  const int c0 = cs_[lo], nch = cs_[lo + 1] - c0;
+  const int c0 = cs_[lo];
+  int nch = cs_[lo + 1] - c0;
+  if (!in_bounds(a.err, nch - 1, INT32_MAX)) nch = 1;
   const int local = u - nbu * c0;
   const int o0 = os[lo], cnt = os[lo + 1] - o0;
   const int cs = (cnt + nch - 1) / nch;
@@ -155,6 +158,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
   U.nb = (local / nch) * mt;
   U.row0 = o0 + c * cs;
   U.ntok = min(cs, cnt - c * cs);
+  // Bounds-checked build: a unit outside the expert-major rows, or larger
+  // than a chunk, records BOUNDS and shrinks to row 0 alone, so that every
+  // role still walks the same (in-bounds) schedule.
+  if (!(in_bounds(a.err, U.e, a.E) && in_bounds(a.err, U.ntok - 1, max_tok) &&
+        in_bounds(a.err, U.row0, a.rows) && in_bounds(a.err, U.row0 + U.ntok - 1, a.rows))) {
+    U.row0 = 0;
+    U.ntok = 1;
+  }
   return U;
 }
 
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
         const int tiles = min(MT, a.nblocks - U.nb);
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
@@ -289,7 +300,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       uint32_t n = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
         const int nbox = (U.ntok + C::kBoxRows - 1) / C::kBoxRows;
         constexpr uint32_t kBoxBytes = C::kBoxRows * 128u;
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       const uint64_t adesc0 = sw128_kmajor_desc(sbase + C::kAOff);
       const uint64_t bdesc0 = sw128_kmajor_desc(sbase + C::kBOff);
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
         const int tiles = min(MT, a.nblocks - U.nb);
         const uint32_t nn = static_cast<uint32_t>((U.ntok + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, nn);
@@ -401,18 +412,19 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t smul2 = a.smul * 0x10001u, sadd2 = a.sadd * 0x10001u;
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol;
+    const uint32_t t_st = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kATmemCol +
+                          static_cast<uint32_t>(grp) * 64u;
+    uint32_t pha = 0;
     uint32_t n = 0;                   // K steps of this CTA before the unit
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       for (int ks = 2 * ((grp - static_cast<int>(n >> 1)) & 3); ks < a.ksteps; ks += 8) {
-        // CTA-wide pair index: weight stage m % SF, A stage m % SAa.
+        // CTA-wide pair index m (m = grp mod 4): weight stage m % SF.
         const uint32_t m = (n + static_cast<uint32_t>(ks)) >> 1;
-        const int sf = static_cast<int>(m % SF), sa = static_cast<int>(m % SAa);
-        const uint32_t phf = (m / SF) & 1u, pha = (m / SAa) & 1u;
-        const uint32_t t_st = t_row + static_cast<uint32_t>(sa) * 64u;
+        const int sf = static_cast<int>(m % SF);
+        const uint32_t phf = (m / SF) & 1u;
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        if (!mbar_wait(emptyA(sa), pha ^ 1u)) { ok = false; break; }
+        if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
         tc_fence_after();             // after the MMA that last read this stage
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -451,7 +463,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aready(sa));
+        if (lane == 0) mbar_arrive(aready(grp));
+        pha ^= 1u;
       }
       n += static_cast<uint32_t>(a.ksteps);
     }
@@ -473,7 +486,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     uint32_t n = 0;                   // global K-step counter of this CTA
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const bool live = decode_unit(a, nbu, MT, tab_cs, tab_os, u).nb + tile < a.nblocks;
+      const bool live = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u).nb + tile < a.nblocks;
       for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
         const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SAa);
         const uint32_t phf = (n / SF) & 1u, pha = (n / SAa) & 1u;
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     uint32_t n_unit = 0;              // K steps of this CTA before the unit
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, n_unit += a.ksteps) {
-      const Unit U = decode_unit(a, nbu, MT, tab_cs, tab_os, u);
+      const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
       if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
@@ -586,7 +599,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       if (MT > 1) {
         // Items (tile, pair of chunks), tiles interleaved, taken round robin
         // by the kParts warps of this lane quarter; one TMEM load and wait
-        // per item (32 columns).
+        // per item (32 columns).  (Releasing each tile on its own gained
+        // nothing: the two tiles' MMA warps share the activation ring.)
         const int npairs = (nchunks + 1) >> 1;
         for (int it = part; it < 2 * npairs; it += kParts) {
           const int tile = it & 1, j = 2 * (it >> 1);

@@ -83,12 +83,15 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const MxGemmArgs& a, int nbu, const int* cs_,
                                             const int* os, int u) {
+  constexpr int max_tok = kMxChunk;
   int lo = 0, hi = a.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (nbu * cs_[mid] <= u) lo = mid; else hi = mid;
   }
-  const int c0 = cs_[lo], nch = cs_[lo + 1] - c0;
+  const int c0 = cs_[lo];
+  int nch = cs_[lo + 1] - c0;
+  if (!in_bounds(a.err, nch - 1, INT32_MAX)) nch = 1;
   const int local = u - nbu * c0;
   const int o0 = os[lo], cnt = os[lo + 1] - o0;
   const int cs = (cnt + nch - 1) / nch;
@@ -98,6 +101,14 @@ __device__ __forceinline__ Unit decode_unit(const MxGemmArgs& a, int nbu, const 
   U.nb = local / nch;          // FC1: block of 128 columns; FC2: pair of row blocks
   U.row0 = o0 + c * cs;
   U.ntok = min(cs, cnt - c * cs);
+  // Bounds-checked build: a unit outside the expert-major rows, or larger
+  // than a chunk, records BOUNDS and shrinks to row 0 alone, so that every
+  // role still walks the same (in-bounds) schedule.
+  if (!(in_bounds(a.err, U.e, a.E) && in_bounds(a.err, U.ntok - 1, max_tok) &&
+        in_bounds(a.err, U.row0, a.rows) && in_bounds(a.err, U.row0 + U.ntok - 1, a.rows))) {
+    U.row0 = 0;
+    U.ntok = 1;
+  }
   return U;
 }
 

@@ -50,11 +50,11 @@ cudaError_t launch_scan(int T, int E, const int32_t* hist, int32_t* base,
 cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
                            const int32_t* base, int32_t* perm, int32_t* inv,
                            const void* x, const uint8_t* xs, int K,
-                           int act_mode, uint16_t* xperm, cudaStream_t st);
+                           int act_mode, uint16_t* xperm, int* err, cudaStream_t st);
 
 // S7: y[t] = sum_j w[t,j] * o[inv[t,j]] -> bf16.
 cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
-                           int T, int k, int K, uint16_t* y, cudaStream_t st);
+                           int T, int k, int K, uint16_t* y, int* err, cudaStream_t st);
 
 // S0: pack one weight matrix [E, N, Kd] into tiles.  gated: FC1 gate/up
 // interleave with `layout` giving the source half order.  bmax: per-expert
@@ -79,6 +79,7 @@ struct GemmArgs {
   const int32_t* cstart;   // [E+1] token-chunk prefix
   void* out;               // FC1: h [P, N/2]; FC2: o f32 [P, N]
   int* err;
+  int64_t rows;            // P: rows of the expert-major buffers
   int E, nblocks, ksteps, tile_bytes, gran;
   uint32_t smul, sadd;     // scale code -> bf16 bits
   int ldo;                 // output row stride in elements
@@ -106,6 +107,7 @@ struct MxGemmArgs {
   void* out;               // FC1: h E4M3 [P, ldo]; FC2: o f32 [P, ldo]
   uint8_t* hscale;         // FC1: h scale words [I/128][hscale_pitch]
   int* err;
+  int64_t rows;            // P: rows of the expert-major buffers
   int E, nblocks, ksteps, rows_per_expert, tiles_per_expert;
   int64_t xscale_pitch, hscale_pitch;  // words per step row
   int ldo;
@@ -123,7 +125,7 @@ cudaError_t launch_mx_scales(const uint8_t* s, int E, int N, int Kd, bool gated,
 // scale words to xsperm [K/128][pitch].
 cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
                              const uint8_t* xs, int K, int64_t pitch, uint8_t* xperm,
-                             uint32_t* xsperm, cudaStream_t st);
+                             uint32_t* xsperm, int* err, cudaStream_t st);
 // Tensor maps of one block-scaled GEMM: the weights (16U4_ALIGN16B, 128 x
 // 128 boxes) and the activation rows with boxes of 32, 64, ..., 256 rows
 // (E4M3, 128-byte swizzle).
@@ -150,5 +152,8 @@ int device_sm_count();
 // mbarrier that nothing completes, and records TIMEOUT in *err.
 cudaError_t launch_wait_timeout(unsigned long long limit_ns, int* err,
                                 cudaStream_t st);
+// Test helper: one write of slot `index` of a 64-entry device array through
+// the index check; out of range records BOUNDS in *err and writes nothing.
+cudaError_t launch_bounds_check(int64_t index, int* err, cudaStream_t st);
 
 }  // namespace fp4moe

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(1024) route_kernel(
     float sum = ex;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < k) {
+    if (lane < k && in_bounds(err, my_id, E)) {
       ids[static_cast<int64_t>(t) * k + lane] = my_id;
       w[static_cast<int64_t>(t) * k + lane] = ex / sum;
       atomicAdd(&cnt[my_id], 1);
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(
 __global__ void __launch_bounds__(512) scatter_kernel(
     const int32_t* __restrict__ ids, int T, int E, int k,
     const int32_t* __restrict__ base, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv) {
+    int32_t* __restrict__ inv, int* err) {
   extern __shared__ int wcnt[];   // [16 warps][E]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t P = static_cast<int64_t>(T) * k;
@@ -383,8 +383,9 @@ __global__ void __launch_bounds__(512) scatter_kernel(
   const int np = static_cast<int>(min(P - p0, static_cast<int64_t>(kTokPerBlk) * k));
   for (int i = tid; i < 16 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  const bool act = tid < np;
+  bool act = tid < np;
   const int e = act ? ids[p0 + tid] : -1;
+  if (act && !in_bounds(err, e, E)) act = false;
   const unsigned m = __match_any_sync(kFull, e);
   const int rank = __popc(m & ((1u << lane) - 1u));
   if (act && rank == 0) wcnt[warp * E + e] = __popc(m);
@@ -393,8 +394,10 @@ __global__ void __launch_bounds__(512) scatter_kernel(
     int pre = 0;
     for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E + e];
     const int pos = base[static_cast<int64_t>(blockIdx.x) * E + e] + pre + rank;
-    perm[pos] = static_cast<int32_t>(p0 + tid);
-    inv[p0 + tid] = pos;
+    if (in_bounds(err, pos, P)) {
+      perm[pos] = static_cast<int32_t>(p0 + tid);
+      inv[p0 + tid] = pos;
+    }
   }
 }
 
@@ -403,10 +406,13 @@ __global__ void __launch_bounds__(512) scatter_kernel(
 // dequantized exactly on the way.
 __global__ void __launch_bounds__(256) gather_kernel(
     const int32_t* __restrict__ inv, int64_t P, int k, const void* __restrict__ x,
-    const uint8_t* __restrict__ xs, int K, int act_mode, uint16_t* __restrict__ xperm) {
+    const uint8_t* __restrict__ xs, int K, int act_mode, uint16_t* __restrict__ xperm,
+    int* err) {
   for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
     const int64_t t = p / k;
-    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<int64_t>(inv[p]) * K);
+    const int64_t row = inv[p];
+    if (!in_bounds(err, row, P)) continue;
+    uint4* dst = reinterpret_cast<uint4*>(xperm + row * K);
     if (act_mode == FP4MOE_ACT_BF16) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + t * K);
       for (int c = threadIdx.x; c < K / 8; c += blockDim.x) dst[c] = __ldg(src + c);
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(256) gather_kernel(
 
 __global__ void __launch_bounds__(256) combine_kernel(
     const float* __restrict__ o, const int32_t* __restrict__ inv,
-    const float* __restrict__ w, int k, int K, uint16_t* __restrict__ y) {
+    const float* __restrict__ w, int k, int K, uint16_t* __restrict__ y, int* err) {
   const int64_t t = blockIdx.x;
   int pos[kMaxTopK];
   float wt[kMaxTopK];
@@ -444,6 +450,8 @@ __global__ void __launch_bounds__(256) combine_kernel(
     if (j < k) {
       pos[j] = inv[t * k + j];
       wt[j] = w[t * k + j];
+      // bounds-checked build: a slot outside [0, P) reads row 0 instead
+      if (!in_bounds(err, pos[j], static_cast<int64_t>(gridDim.x) * k)) pos[j] = 0;
     }
   }
   for (int n = threadIdx.x * 8; n < K; n += blockDim.x * 8) {
@@ -679,10 +687,11 @@ __global__ void __launch_bounds__(256) mx_scales_kernel(
 __global__ void __launch_bounds__(256) gather_mx_kernel(
     const int32_t* __restrict__ inv, int64_t P, int k, const uint8_t* __restrict__ x,
     const uint8_t* __restrict__ xs, int K, int64_t pitch, uint8_t* __restrict__ xperm,
-    uint32_t* __restrict__ xsperm) {
+    uint32_t* __restrict__ xsperm, int* err) {
   for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
     const int64_t t = p / k;
     const int64_t row = inv[p];
+    if (!in_bounds(err, row, P) || !in_bounds(err, row, pitch)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
     uint4* dst = reinterpret_cast<uint4*>(xperm + row * K);
     for (int c = threadIdx.x; c < K / 16; c += blockDim.x) dst[c] = __ldg(src + c);
@@ -759,7 +768,7 @@ cudaError_t launch_scan(int T, int E, const int32_t* hist, int32_t* base,
 cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
                            const int32_t* base, int32_t* perm, int32_t* inv,
                            const void* x, const uint8_t* xs, int K,
-                           int act_mode, uint16_t* xperm, cudaStream_t st) {
+                           int act_mode, uint16_t* xperm, int* err, cudaStream_t st) {
   const int nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
   if (nblk == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(16) * E * sizeof(int);
@@ -769,12 +778,12 @@ cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv);
+  scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || xperm == nullptr) return e;
   const int64_t P = static_cast<int64_t>(T) * k;
   const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
-  gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm);
+  gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm, err);
   return cudaGetLastError();
 }
 
@@ -800,18 +809,18 @@ cudaError_t launch_mx_scales(const uint8_t* s, int E, int N, int Kd, bool gated,
 
 cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
                              const uint8_t* xs, int K, int64_t pitch, uint8_t* xperm,
-                             uint32_t* xsperm, cudaStream_t st) {
+                             uint32_t* xsperm, int* err, cudaStream_t st) {
   const int64_t P = static_cast<int64_t>(T) * k;
   if (P == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
-  gather_mx_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, pitch, xperm, xsperm);
+  gather_mx_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, pitch, xperm, xsperm, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
-                           int T, int k, int K, uint16_t* y, cudaStream_t st) {
+                           int T, int k, int K, uint16_t* y, int* err, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 256, 0, st>>>(o, inv, w, k, K, y);
+  combine_kernel<<<T, 256, 0, st>>>(o, inv, w, k, K, y, err);
   return cudaGetLastError();
 }
 

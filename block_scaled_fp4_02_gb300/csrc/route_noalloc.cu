@@ -84,6 +84,6 @@ extern "C" int fp4moe_route_noalloc(const float* logits, int T, int E,
     e = launch_scan(T, E, hist, base, counts, offsets, cstart, gemm_chunk_max(T), st);
   if (e == cudaSuccess)
     e = launch_scatter(ids, T, E, top_k, base, perm, inv, nullptr, nullptr, 0,
-                       FP4MOE_ACT_BF16, nullptr, st);
+                       FP4MOE_ACT_BF16, nullptr, status_word(), st);
   return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA;
 }

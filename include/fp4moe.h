@@ -42,7 +42,9 @@ enum fp4moe_status {
   FP4MOE_ERR_UNSUPPORTED = 2,         /* valid request this build refuses   */
   FP4MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below the *_size() query  */
   FP4MOE_ERR_CUDA = 4,                /* a CUDA runtime call failed         */
-  FP4MOE_ERR_TIMEOUT = 5              /* a bounded device wait gave up      */
+  FP4MOE_ERR_TIMEOUT = 5,             /* a bounded device wait gave up      */
+  FP4MOE_ERR_BOUNDS = 6               /* an index check of the bounds-checked
+                                         build failed (the access was skipped) */
 };
 
 /* Row order of the fused FC1 weight w13 [E, 2I, K].  "w31"/gate_up is the
@@ -297,6 +299,25 @@ int fp4moe_route_noalloc(const float* logits, int T, int E, int top_k,
  * fp4moe_last_device_error() then returns.  Every wait inside the library's
  * kernels is bounded the same way (about 2 s).  Asynchronous on `stream`. */
 int fp4moe_test_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Build variant (no counterpart on the pages).  The library is built twice
+ * from the same sources: libfp4moe.so and libfp4moe_checked.so, the latter
+ * compiled with FP4MOE_BOUNDS_CHECK, where every data-dependent index (expert
+ * ids, permutation slots, work-unit rows and columns, scale offsets) is
+ * checked against its buffer before the access; a failed check records
+ * FP4MOE_ERR_BOUNDS in the device status word and skips the access (a
+ * GEMM work unit with a bad expert index is computed from expert 0 and its
+ * stores are checked as well).  Returns FP4MOE_BUILD_BOUNDS_CHECK in the
+ * checked build, 0 otherwise. */
+#define FP4MOE_BUILD_BOUNDS_CHECK 1
+int fp4moe_build_flags(void);
+
+/* Test export of the index check (no counterpart on the pages): one thread
+ * writes slot `index` of a 64-entry device array through the same check the
+ * checked build applies (in both builds); an index outside [0, 64) records
+ * FP4MOE_ERR_BOUNDS in the device status word and writes nothing.
+ * Asynchronous on `stream`. */
+int fp4moe_test_bounds_check(int64_t index, void* stream);
 
 /* Static text for a status code (never NULL); see the status codes above. */
 const char* fp4moe_status_string(int status);

@@ -25,8 +25,33 @@ def test_exports_every_header_symbol(lib):
 def test_status_strings(lib):
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported"),
                        (3, "workspace too small"), (4, "CUDA error"),
-                       (5, "device wait timed out"), (99, "unknown status")]:
+                       (5, "device wait timed out"),
+                       (6, "index out of bounds (bounds-checked build)"),
+                       (99, "unknown status")]:
         assert lib.fp4moe_status_string(code).decode() == text
+
+
+def test_bounds_checked_variant_builds_and_exports_every_symbol():
+    # The same sources compiled with FP4MOE_BOUNDS_CHECK; both variants say
+    # which they are (a host-only call).
+    import importlib
+    b = importlib.import_module("block_scaled_fp4_02_gb300.build")
+    path = fp4.build(variant_name="checked")
+    assert path == b.lib_path("checked") and path != b.lib_path("release")
+    checked = ctypes.CDLL(path)
+    missing = [n for n in fp4.exported_symbols() if not hasattr(checked, n)]
+    assert not missing, missing
+    assert checked.fp4moe_build_flags() == fp4.BUILD_BOUNDS_CHECK
+    assert ctypes.CDLL(b.lib_path("release")).fp4moe_build_flags() == 0
+
+
+def test_variant_follows_the_environment(monkeypatch):
+    monkeypatch.delenv("FP4MOE_BOUNDS_CHECK", raising=False)
+    assert fp4.variant() == "release"
+    monkeypatch.setenv("FP4MOE_BOUNDS_CHECK", "0")
+    assert fp4.variant() == "release"
+    monkeypatch.setenv("FP4MOE_BOUNDS_CHECK", "1")
+    assert fp4.variant() == "checked"
 
 
 FAKE = 0x10000  # an aligned non-null address; never dereferenced on the host

@@ -18,6 +18,8 @@ def _gpu():
     assert torch.cuda.is_available(), "these tests need a CUDA GPU"
     fp4.build()
     fp4.load()
+    assert fp4.build_flags() == (fp4.BUILD_BOUNDS_CHECK
+                                 if fp4.variant() == "checked" else 0)
     assert fp4.last_device_error() == fp4.OK
 
 
@@ -209,3 +211,21 @@ def test_bounded_wait_gives_up_and_records_timeout():
     codes, scales, _ = synth.requant_inputs(synth.SMALL_REQUANT)
     gpu_requant(codes, scales)
     assert fp4.last_device_error() == fp4.OK
+
+
+# ------------------------------------------------------------- index checks
+
+@pytest.mark.parametrize("index,expect", [(0, fp4.OK), (63, fp4.OK),
+                                          (64, fp4.ERR_BOUNDS),
+                                          (-1, fp4.ERR_BOUNDS),
+                                          (1 << 40, fp4.ERR_BOUNDS)])
+def test_index_check_records_bounds_and_skips_the_access(index, expect):
+    # The check the bounds-checked build applies to every data-dependent
+    # index, run on a 64-entry array: out of range it records BOUNDS and
+    # writes nothing (the context stays usable).
+    assert fp4.last_device_error() == fp4.OK
+    fp4.test_bounds_check(index)
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == expect
+    x = torch.arange(64, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 2016.0

@@ -20,6 +20,8 @@ def _gpu():
     assert torch.cuda.is_available(), "these tests need a CUDA GPU"
     fp4.build()
     fp4.load()
+    assert fp4.build_flags() == (fp4.BUILD_BOUNDS_CHECK
+                                 if fp4.variant() == "checked" else 0)
     assert fp4.last_device_error() == fp4.OK
 
 
