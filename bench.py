@@ -364,6 +364,15 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src):
            "tflops": tflops, "weight_gbs": wgbs,
            "touched_experts": run.touched, "stage_ms": stages}
     tensor_bound = P / cfg.E >= 64
+    # The FC1 kernel this workload runs: the block-scaled kernel for FP8
+    # activations over group32 weights, else the CTA-pair kernel for chunks
+    # of up to 256 tokens (T > 64), else the one-CTA 32-token variant.
+    if run.mx:
+        kname = "moe_gemm_mx_kernel<FC1> (FC1 + SwiGLU, block-scaled FP8 x FP4)"
+    elif cfg.T > 64:
+        kname = "moe_gemm_pair_kernel<FC1> (FC1 + SwiGLU, CTA pairs)"
+    else:
+        kname = "moe_gemm_kernel<32, FC1> (FC1 + SwiGLU)"
     peak, bf16 = tensor_peak(pk, run.fp8)
     pname = ("2 x measured bf16_tflops (FP8 dense)" if run.fp8 else
              "bf16_tflops (burst)")
@@ -372,7 +381,7 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src):
         roof = {"bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_source": f"{pk_src} {pname}",
-                "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
+                "kernel": kname,
                 "per_launch_flops": fc1_flops,
                 "per_launch_bytes": run.fc1_bytes()}
         fc2 = fc2_flops / (fc2_ms / 1e3) / 1e12
@@ -387,7 +396,7 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src):
         ach = run.fc1_bytes() / (fc1_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "peak_source": f"{pk_src} hbm_gbs",
-                "kernel": "moe_gemm_kernel (FC1 + SwiGLU)",
+                "kernel": kname,
                 "per_launch_bytes": run.fc1_bytes()}
         fc2 = run.fc2_bytes() / (fc2_ms / 1e3) / 1e9
         out["fc2_roofline"] = {"bound": "hbm", "achieved": fc2, "peak": hbm,

@@ -592,11 +592,6 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
   stage_mark(3, st);
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 
-  CUtensorMap tm_x, tm_h;
-  const uint32_t box_rows = static_cast<uint32_t>(gemm_box_rows(chunk));
-  if (!make_row_tmap(&tm_x, xperm, P, p->K, box_rows) ||
-      !make_row_tmap(&tm_h, h, P, p->I, box_rows))
-    return FP4MOE_ERR_CUDA;
   GemmArgs a1{};
   a1.wpack = p->w13; a1.alpha = p->alpha; a1.offsets = offsets; a1.cstart = cstart;
   a1.err = err; a1.rows = P; a1.E = p->E; a1.nblocks = 2 * p->I / kTileN;
@@ -610,15 +605,26 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
     a1.out = h32;
     a1.mode = kGemmModeFc1Fp8;
   }
-  e = launch_gemm(tm_x, a1, chunk, sms, st);
+  GemmArgs a2 = a1;
+  a2.wpack = p->w2; a2.alpha = p->alpha + p->E; a2.nblocks = p->K / kTileN;
+  a2.ksteps = p->I / kTileK; a2.out = o; a2.ldo = p->K; a2.mode = kGemmModeFc2;
+  // Many tokens per expert: the CTA-pair kernel where the block and step
+  // counts split evenly, else the one-CTA kernel.  Each has its own box rows.
+  const bool pair1 = chunk > 32 && gemm_pair_supported(a1);
+  const bool pair2 = chunk > 32 && gemm_pair_supported(a2);
+  CUtensorMap tm_x, tm_h;
+  if (!make_row_tmap(&tm_x, xperm, P, p->K,
+                     static_cast<uint32_t>(pair1 ? kPairBoxRows : gemm_box_rows(chunk))) ||
+      !make_row_tmap(&tm_h, h, P, p->I,
+                     static_cast<uint32_t>(pair2 ? kPairBoxRows : gemm_box_rows(chunk))))
+    return FP4MOE_ERR_CUDA;
+  e = pair1 ? launch_gemm_pair(tm_x, a1, sms, st) : launch_gemm(tm_x, a1, chunk, sms, st);
   stage_mark(4, st);
   if (e == cudaSuccess && p->act_mode == FP4MOE_ACT_FP8)
     e = launch_h_fp8_round(h32, P, p->I, h, st);
   stage_mark(5, st);
-  GemmArgs a2 = a1;
-  a2.wpack = p->w2; a2.alpha = p->alpha + p->E; a2.nblocks = p->K / kTileN;
-  a2.ksteps = p->I / kTileK; a2.out = o; a2.ldo = p->K; a2.mode = kGemmModeFc2;
-  if (e == cudaSuccess) e = launch_gemm(tm_h, a2, chunk, sms, st);
+  if (e == cudaSuccess)
+    e = pair2 ? launch_gemm_pair(tm_h, a2, sms, st) : launch_gemm(tm_h, a2, chunk, sms, st);
   stage_mark(6, st);
   if (e == cudaSuccess)
     e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), err, st);

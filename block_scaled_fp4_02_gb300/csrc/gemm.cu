@@ -45,6 +45,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_parts.cuh"
 #include "internal.h"
 
 namespace fp4moe {
@@ -130,62 +131,6 @@ struct Cfg {
   static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kBStage % 1024 == 0,
                 "swizzled operands need 1 KB alignment");
 };
-
-struct Unit {
-  int e, nb, row0, ntok;   // nb: first 128-row weight block of the unit
-};
-
-// Units are ordered (expert, weight-block group, token chunk); expert e owns
-// nbu * (cstart[e+1] - cstart[e]) consecutive units, nbu = ceil(nblocks/MT).
-// cs_/os are the shared-memory copies of cstart and offsets.
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
-                                            int mt, int max_tok, const int* cs_,
-                                            const int* os, int u) {
-  int lo = 0, hi = a.E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (nbu * cs_[mid] <= u) lo = mid; else hi = mid;
-  }
-  const int c0 = cs_[lo];
-  int nch = cs_[lo + 1] - c0;
-  if (!in_bounds(a.err, nch - 1, INT32_MAX)) nch = 1;
-  const int local = u - nbu * c0;
-  const int o0 = os[lo], cnt = os[lo + 1] - o0;
-  const int cs = (cnt + nch - 1) / nch;
-  const int c = local % nch;
-  Unit U;
-  U.e = lo;
-  U.nb = (local / nch) * mt;
-  U.row0 = o0 + c * cs;
-  U.ntok = min(cs, cnt - c * cs);
-  // Bounds-checked build: a unit outside the expert-major rows, or larger
-  // than a chunk, records BOUNDS and shrinks to row 0 alone, so that every
-  // role still walks the same (in-bounds) schedule.
-  if (!(in_bounds(a.err, U.e, a.E) && in_bounds(a.err, U.ntok - 1, max_tok) &&
-        in_bounds(a.err, U.row0, a.rows) && in_bounds(a.err, U.row0 + U.ntok - 1, a.rows))) {
-    U.row0 = 0;
-    U.ntok = 1;
-  }
-  return U;
-}
-
-// 8 packed E2M1 codes -> 8 bf16 (4 words, element 0 in the low half of
-// word 0), each multiplied by the bf16 pair s2.  The packer places each
-// element's magnitude bits (m, e0, e1) and sign so that shifts and masks put
-// them at bf16 bits 6..8 and 15 (or 22..24 and 31): read as bf16, (s, e1, e0,
-// m) there is e2m1 * 2^-126 (code 1 = 0.5 lands on a subnormal), and the
-// multiply by s * 2^119 gives e2m1 * s * 2^-7 exactly.  Plain shifts (no
-// rotates) let the compiler put the left shifts on the multiply-add pipe,
-// which is less loaded than the logic pipe.
-__device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t s2) {
-  const uint32_t w0 = x & 0x81C081C0u;
-  const uint32_t w1 = (x << 3) & 0x81C081C0u;
-  const uint32_t w2 = (x << 6) & 0x81C081C0u;
-  const uint32_t w3 = ((x >> 8) & 0x00400040u) | ((x >> 3) & 0x01800180u) |
-                      ((x << 2) & 0x80008000u);
-  return make_uint4(bf16x2_mul(w0, s2), bf16x2_mul(w1, s2), bf16x2_mul(w2, s2),
-                    bf16x2_mul(w3, s2));
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
@@ -424,10 +369,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const int sf = static_cast<int>(m % SF);
         const uint32_t phf = (m / SF) & 1u;
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
-        tc_fence_after();             // after the MMA that last read this stage
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        // Converts weight tile t of the stage: the 16 words of K columns
+        // 0..31 into va and those of 32..63 into vb.
+        auto convert = [&](int t, uint32_t (&va)[16], uint32_t (&vb)[16]) {
           const uint8_t* f = smem + C::kFOff + sf * C::kFStage + t * a.tile_bytes;
           const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
           const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
@@ -443,21 +387,30 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             s0 = s1 = sc[0] * smul2 + sadd2;
             s2 = s3 = sc[1] * smul2 + sadd2;
           }
-          {
-            const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
-            const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
-            const uint32_t v[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                    w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-            tmem_st16(t_st + t * 32u, v);
+          const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
+          const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
+          const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
+          const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
+          const uint4 wa[4] = {w0, w1, w2, w3}, wb[4] = {w4, w5, w6, w7};
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            va[4 * x] = wa[x].x; va[4 * x + 1] = wa[x].y;
+            va[4 * x + 2] = wa[x].z; va[4 * x + 3] = wa[x].w;
+            vb[4 * x] = wb[x].x; vb[4 * x + 1] = wb[x].y;
+            vb[4 * x + 2] = wb[x].z; vb[4 * x + 3] = wb[x].w;
           }
-          {
-            const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
-            const uint4 w6 = dequant8(d1.z, s3), w7 = dequant8(d1.w, s3);
-            const uint32_t v[16] = {w4.x, w4.y, w4.z, w4.w, w5.x, w5.y, w5.z, w5.w,
-                                    w6.x, w6.y, w6.z, w6.w, w7.x, w7.y, w7.z, w7.w};
-            tmem_st16(t_st + t * 32u + 16u, v);
-          }
-        }
+        };
+        // The first tile is converted before waiting for the A stage, so
+        // the conversion overlaps the MMAs that still read the stage.
+        uint32_t va[16], vb[16];
+        convert(0, va, vb);
+        if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
+        tc_fence_after();             // after the MMA that last read this stage
+        tmem_st16(t_st, va);
+        tmem_st16(t_st + 16u, vb);
+        convert(1, va, vb);
+        tmem_st16(t_st + 32u, va);
+        tmem_st16(t_st + 48u, vb);
         __syncwarp();
         if (lane == 0) mbar_arrive(emptyF(sf));
         tmem_st_wait();

@@ -91,6 +91,13 @@ constexpr int kGemmModeFc1 = 0, kGemmModeFc2 = 1, kGemmModeFc1Fp8 = 2;
 
 cudaError_t launch_gemm(const CUtensorMap& tmB, const GemmArgs& a, int nt,
                         int num_sms, cudaStream_t st);
+// The same GEMM on CTA pairs (tcgen05 cta_group::2, chunks of up to 256
+// tokens, activation boxes of kPairBoxRows rows): for an even number of
+// 128-row blocks and of K steps.
+constexpr int kPairBoxRows = 128;
+bool gemm_pair_supported(const GemmArgs& a);
+cudaError_t launch_gemm_pair(const CUtensorMap& tmB, const GemmArgs& a, int num_sms,
+                             cudaStream_t st);
 
 // S5 / S6 on the block-scaled path (FP8 activations over group32 weights):
 // kind::mxf8f6f4, E2M1 weights widened by TMA, E4M3 rows, UE8M0 scales.
