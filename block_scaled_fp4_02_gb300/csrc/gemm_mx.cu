@@ -58,7 +58,11 @@ constexpr uint32_t kSfbBytes = (kMxChunk256Rows + 16) * 4;
 constexpr uint32_t kOffA = 0, kOffB = 2 * kATile, kOffSfa = kOffB + kBBytes,
                    kOffSfb = kOffSfa + 2 * kSfaBytes;
 constexpr uint32_t kStage = (kOffSfb + kSfbBytes + 1023) & ~1023u;
-constexpr int kNumBars = 2 * kStages + 2 * kMxSfSlots + 2 + 1;
+// Barriers per stage: full (TMA bytes), ready (scale factors of the stage in
+// its TMEM slot: implies full), empty (both MMA issuers' commits: frees the
+// shared-memory stage and its scale slot).
+constexpr int kNumBars = 3 * kStages + 2 + 1;
+static_assert(kStages <= kMxSfSlots, "one TMEM scale slot per stage");
 constexpr uint32_t kBarOff = kStage * kStages;
 constexpr uint32_t kTabOff = kBarOff + 8 * kNumBars + 16;
 constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
@@ -127,9 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + kBarOff;
   auto fullS = [&](int s) { return bars + 8u * s; };
   auto emptyS = [&](int s) { return bars + 8u * (kStages + s); };
-  auto sfReady = [&](int j) { return bars + 8u * (2 * kStages + j); };
-  auto sfEmpty = [&](int j) { return bars + 8u * (2 * kStages + kMxSfSlots + j); };
-  const uint32_t accFull = bars + 8u * (2 * kStages + 2 * kMxSfSlots);
+  auto readyS = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  const uint32_t accFull = bars + 8u * (3 * kStages);
   const uint32_t accEmpty = accFull + 8u;
   const uint32_t done_bar = accFull + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
@@ -145,11 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(fullS(s), 2);     // weight and activation producers
+      mbar_init(readyS(s), 4);    // four scale warps
       mbar_init(emptyS(s), 2);    // both MMA issuers
-    }
-    for (int j = 0; j < kMxSfSlots; ++j) {
-      mbar_init(sfReady(j), 4);   // four scale warps
-      mbar_init(sfEmpty(j), 2);   // both MMA issuers
     }
     mbar_init(accFull, 2);
     mbar_init(accEmpty, kEpiWarps);
@@ -228,10 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(accEmpty, acc_ph ^ 1u)) { ok = false; break; }
         tc_fence_after();
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
+          // One wait per step: the scale warps arrive on ready(s) only after
+          // the stage's copies landed (full(s)) and its scales are in TMEM.
           const int s = static_cast<int>(n % kStages);
-          const int j = static_cast<int>(n % kMxSfSlots);
-          if (!mbar_wait(fullS(s), (n / kStages) & 1u) ||
-              !mbar_wait(sfReady(j), (n / kMxSfSlots) & 1u)) {
+          if (!mbar_wait(readyS(s), (n / kStages) & 1u)) {
             ok = false;
             break;
           }
@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = sbase + s * kStage;
             const uint64_t ad = desc_at(st + kOffA + t * kATile);
             const uint64_t bd = desc_at(st + kOffB);
-            const uint32_t sfa = tmem + sf_col(j) + 4u * t;
-            const uint32_t sfb = tmem + sf_col(j) + 8u;
+            const uint32_t sfa = tmem + sf_col(s) + 4u * t;
+            const uint32_t sfb = tmem + sf_col(s) + 8u;
 #pragma unroll
             for (int kk = 0; kk < kMxK / 32; ++kk)
               umma_mx(d_tmem, ad + 2u * kk, bd + 2u * kk,
@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (ks > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(emptyS(s));
-          umma_commit(sfEmpty(j));
         }
         if (!ok) break;
         umma_commit(accFull);
@@ -273,10 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tiles = (MODE == kGemmModeFc2) ? min(2, a.nblocks - 2 * U.nb) : 2;
       const int lead = U.row0 & 3;
       for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
+        // The stage's scale slot is free: the producers reloaded the stage,
+        // which needed the MMAs that last read the slot to complete.
         const int s = static_cast<int>(n % kStages);
-        const int j = static_cast<int>(n % kMxSfSlots);
-        if (!mbar_wait(fullS(s), (n / kStages) & 1u) ||
-            !mbar_wait(sfEmpty(j), ((n / kMxSfSlots) & 1u) ^ 1u)) {
+        if (!mbar_wait(fullS(s), (n / kStages) & 1u)) {
           ok = false;
           break;
         }
@@ -285,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* sfa = reinterpret_cast<const uint32_t*>(st + kOffSfa);
         const uint32_t* sfb = reinterpret_cast<const uint32_t*>(st + kOffSfb) + lead;
         const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t col = tmem + lanes + sf_col(j);
+        const uint32_t col = tmem + lanes + sf_col(s);
         for (int t = 0; t < tiles; ++t) tmem_st1(col + 4u * t + q, sfa[t * 128 + 32 * q + lane]);
         uint32_t v[8];
 #pragma unroll
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfReady(j));
+        if (lane == 0) mbar_arrive(readyS(s));
       }
     }
     if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
