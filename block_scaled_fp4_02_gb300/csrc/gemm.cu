@@ -174,7 +174,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       mbar_init(emptyF(s), C::kDqPerF);
     }
     for (int s = 0; s < SAa; ++s) {
-      mbar_init(aready(s), C::kDqPerStage);
+      // TMEM A: aready(g) also takes the two activation producers' arrivals
+      // (and TMA bytes) of the pair's K steps, so an MMA warp waits on one
+      // barrier per pair.
+      mbar_init(aready(s), C::kDqPerStage + (C::kATmem ? 2 : 0));
       mbar_init(emptyA(s), C::kATmem ? 1 : C::kMmaWarps);
     }
     for (int s = 0; s < SB; ++s) {
@@ -259,20 +262,25 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                           (((n >> 1) / SAa) & 1u) ^ 1u)
               : mbar_wait(emptyB(s), ph ^ 1u);
           if (!fr) { ok = false; break; }
-          mbar_arrive_expect_tx(fullB(s), nbox * kBoxBytes);
+          // Completion barrier: fullB(s), or with TMEM A the pair's aready.
+          const int cb = C::kATmem ? static_cast<int>((n >> 1) % SAa) : s;
+          const uint32_t cph = C::kATmem ? ((n >> 1) / SAa) & 1u : ph;
+          const uint32_t full = C::kATmem ? aready(cb) : fullB(cb);
+          mbar_arrive_expect_tx(full, nbox * kBoxBytes);
           const uint32_t dst = sbase + C::kBOff + s * C::kBStage;
           // Rows past the chunk (up to the box) are loaded but not used;
           // rows past the tensor are zero-filled by the TMA unit.
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(dst + b * kBoxBytes, &tmB, ks * kTileK, U.row0 + C::kBoxRows * b,
-                        fullB(s));
-          issued |= 1u << s;
-          issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                        full);
+          issued |= 1u << cb;
+          issued_ph = (issued_ph & ~(1u << cb)) | (cph << cb);
         }
       }
       if (!ok) record_error(a.err, FP4MOE_ERR_TIMEOUT);
       for (int t = 0; t < SB; ++t)
-        if ((issued >> t) & 1u) mbar_wait(fullB(t), (issued_ph >> t) & 1u);
+        if ((issued >> t) & 1u)
+          mbar_wait(C::kATmem ? aready(t) : fullB(t), (issued_ph >> t) & 1u);
     }
   } else if (C::kATmem ? warp >= C::kWarpMmaX0
                         : (warp == kWarpMma || warp == C::kWarpMmaX0)) {
@@ -304,8 +312,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           const int sa = static_cast<int>(C::kATmem ? m % SAa : n % SAa);
           const uint32_t pa = C::kATmem ? (m / SAa) & 1u : (n / SAa) & 1u;
           const int sb = static_cast<int>(n % SB);
-          if (!mbar_wait(fullB(sb), (n / SB) & 1u) ||
-              (C::kATmem && !mbar_wait(fullB((sb + 1) % SB), ((n + 1) / SB) & 1u)) ||
+          // TMEM A: aready(sa) also covers both K steps' activation rows.
+          if ((!C::kATmem && !mbar_wait(fullB(sb), (n / SB) & 1u)) ||
               !mbar_wait(aready(sa), pa)) {
             ok = false;
             break;
