@@ -364,11 +364,11 @@ def summarize(run: MoeRun, total_ms, stages, steps, pk, pk_src):
            "tflops": tflops, "weight_gbs": wgbs,
            "touched_experts": run.touched, "stage_ms": stages}
     tensor_bound = P / cfg.E >= 64
-    # The FC1 kernel this workload runs: the block-scaled kernel for FP8
-    # activations over group32 weights, else the CTA-pair kernel for chunks
-    # of up to 256 tokens (T > 64), else the one-CTA 32-token variant.
+    # The FC1 kernel this workload runs: the block-scaled CTA-pair kernel for
+    # FP8 activations over group32 weights, else the bf16 CTA-pair kernel for
+    # chunks of up to 256 tokens (T > 64), else the one-CTA 32-token variant.
     if run.mx:
-        kname = "moe_gemm_mx_kernel<FC1> (FC1 + SwiGLU, block-scaled FP8 x FP4)"
+        kname = "moe_gemm_mx_pair_kernel<FC1> (FC1 + SwiGLU, block-scaled FP8 x FP4, CTA pairs)"
     elif cfg.T > 64:
         kname = "moe_gemm_pair_kernel<FC1> (FC1 + SwiGLU, CTA pairs)"
     else:

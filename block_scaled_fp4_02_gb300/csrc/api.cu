@@ -248,7 +248,8 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   a1.rows_per_expert = 2 * p->I; a1.tiles_per_expert = 2 * p->I / 128;
   a1.xscale_pitch = L.pitch; a1.hscale_pitch = L.pitch; a1.ldo = p->I;
   a1.mode = kGemmModeFc1;
-  e = launch_gemm_mx(m1, a1, sms, st);
+  e = gemm_mx_pair_supported(a1) ? launch_gemm_mx_pair(m1, a1, sms, st)
+                                 : launch_gemm_mx(m1, a1, sms, st);
   stage_mark(4, st);
   stage_mark(5, st);
   MxGemmArgs a2 = a1;
@@ -256,7 +257,9 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
   a2.hscale = nullptr; a2.nblocks = p->K / 128; a2.ksteps = p->I / kMxK;
   a2.rows_per_expert = p->K; a2.tiles_per_expert = p->K / 128; a2.ldo = p->K;
   a2.mode = kGemmModeFc2;
-  if (e == cudaSuccess) e = launch_gemm_mx(m2, a2, sms, st);
+  if (e == cudaSuccess)
+    e = gemm_mx_pair_supported(a2) ? launch_gemm_mx_pair(m2, a2, sms, st)
+                                   : launch_gemm_mx(m2, a2, sms, st);
   stage_mark(6, st);
   if (e == cudaSuccess)
     e = launch_combine(o, inv, wts, T, top_k, p->K, static_cast<uint16_t*>(y), err, st);

@@ -354,6 +354,22 @@ __device__ __forceinline__ void umma_f16_ta_pair(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// The block-scaled form over the CTA pair (kind::mxf8f6f4, M = 256): A and
+// B in shared memory as above; each CTA's SFA holds the scales of its own A
+// rows and its SFB those of all N columns (both halves of B), each CTA
+// reading its own TMEM.
+__device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives on the mbarrier at offset `bar` in both CTAs of the pair when the
 // pair MMAs issued so far by this thread complete.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {

@@ -143,6 +143,11 @@ struct MxMaps {
 };
 cudaError_t launch_gemm_mx(const MxMaps& maps, const MxGemmArgs& a, int num_sms,
                            cudaStream_t st);
+// The same GEMM on CTA pairs (tcgen05 cta_group::2): FC1 needs an even
+// number of 128-column blocks, FC2 a number of 128-row blocks divisible by 4.
+bool gemm_mx_pair_supported(const MxGemmArgs& a);
+cudaError_t launch_gemm_mx_pair(const MxMaps& maps, const MxGemmArgs& a, int num_sms,
+                                cudaStream_t st);
 
 // Chunk size (tokens) a GEMM launch for T tokens uses; the scan needs it.
 int gemm_chunk_max(int T);
