@@ -320,7 +320,16 @@ def _sample_tokens(T, n, seed):
     return sorted(s)
 
 
+# Few-token decode at full size (8 and ~32 experts touched), same weights as
+# the decode workload.
+DECODE_T1 = synth.MoeConfig("decode_w4a16_E256_K6144_I2048_T1_k8", 256, 6144, 2048, 1, 8,
+                            weight_seed=1003, input_seed=2021)
+DECODE_T4 = synth.MoeConfig("decode_w4a16_E256_K6144_I2048_T4_k8", 256, 6144, 2048, 4, 8,
+                            weight_seed=1003, input_seed=2022)
+
+
 @pytest.mark.parametrize("cfg,n", [(synth.DECODE, 64), (synth.DECODE_SKEW, 64),
+                                   (DECODE_T1, 1), (DECODE_T4, 4),
                                    (synth.PREFILL, 24), (synth.FP8, 24)],
                          ids=lambda c: getattr(c, "name", str(c)))
 def test_moe_full_size_sampled(orc, cfg, n, record_property):
