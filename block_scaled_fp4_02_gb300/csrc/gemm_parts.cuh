@@ -49,18 +49,18 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int nbu,
 
 // 8 packed E2M1 codes -> 8 bf16 (4 words, element 0 in the low half of
 // word 0), each multiplied by the bf16 pair s2.  The packer places each
-// element's magnitude bits (m, e0, e1) and sign so that shifts and masks put
-// them at bf16 bits 6..8 and 15 (or 22..24 and 31): read as bf16, (s, e1, e0,
-// m) there is e2m1 * 2^-126 (code 1 = 0.5 lands on a subnormal), and the
-// multiply by s * 2^119 gives e2m1 * s * 2^-7 exactly.  Plain shifts (no
-// rotates) let the compiler put the left shifts on the multiply-add pipe,
-// which is less loaded than the logic pipe.
+// element's magnitude bits (m, e0, e1) and sign so that a shift (or rotate)
+// and a mask put them at bf16 bits 6..8 and 15 (or 22..24 and 31): read as
+// bf16, (s, e1, e0, m) there is e2m1 * 2^-126 (code 1 = 0.5 lands on a
+// subnormal), and the multiply by s * 2^119 gives e2m1 * s * 2^-7 exactly.
+// Seven logic operations per eight elements; the compiler can put the two
+// left shifts on the multiply-add pipe, which is less loaded than the logic
+// pipe.
 __device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t s2) {
-  const uint32_t w0 = x & 0x81C081C0u;
-  const uint32_t w1 = (x << 3) & 0x81C081C0u;
-  const uint32_t w2 = (x << 6) & 0x81C081C0u;
-  const uint32_t w3 = ((x >> 8) & 0x00400040u) | ((x >> 3) & 0x01800180u) |
-                      ((x << 2) & 0x80008000u);
+  const uint32_t w0 = ((x >> 8) & 0x00400040u) | (x & 0x81808180u);
+  const uint32_t w1 = (x << 6) & 0x81C081C0u;
+  const uint32_t w2 = __funnelshift_l(x, x, 12) & 0x81C081C0u;
+  const uint32_t w3 = (x << 2) & 0x81C081C0u;
   return make_uint4(bf16x2_mul(w0, s2), bf16x2_mul(w1, s2), bf16x2_mul(w2, s2),
                     bf16x2_mul(w3, s2));
 }

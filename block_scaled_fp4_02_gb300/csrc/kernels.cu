@@ -497,13 +497,15 @@ __global__ void __launch_bounds__(256) combine_kernel(
 // matrix maximum flush to zero).
 
 // Bit positions of element j (k offset 0..7) in a packed word, for its
-// magnitude bits m, e0, e1 (E2M1 bits 0..2) and its sign: elements 0..5 keep
-// their magnitude bits contiguous and the sign 9 bits above them, so one left
-// shift and one mask place two of them as bf16 (s, e1, e0, m) at bits 15, 8,
-// 7, 6 and 31, 24, 23, 22; elements 6 and 7 need three shifts.
+// magnitude bits m, e0, e1 (E2M1 bits 0..2) and its sign.  The dequantizer
+// extracts the four bf16 pairs (s, e1, e0, m at bits 15, 8, 7, 6 and 31, 24,
+// 23, 22) as: elements 0, 1 by one right shift (m) and the word itself (the
+// rest); 2, 3 by a left shift of 6; 4, 5 by a rotate of 12; 6, 7 by a left
+// shift of 2, each followed by one mask: seven logic operations per eight
+// elements, the fewest of any layout with this extraction pattern.
 __constant__ uint8_t kBitPos[8][4] = {
-    {6, 7, 8, 15},   {22, 23, 24, 31}, {3, 4, 5, 12},   {19, 20, 21, 28},
-    {0, 1, 2, 9},    {16, 17, 18, 25}, {14, 10, 11, 13}, {30, 26, 27, 29}};
+    {14, 7, 8, 15},  {30, 23, 24, 31}, {0, 1, 2, 9},    {16, 17, 18, 25},
+    {26, 27, 28, 3}, {10, 11, 12, 19}, {4, 5, 6, 13},   {20, 21, 22, 29}};
 
 __device__ __forceinline__ uint32_t pack8(const uint8_t* c) {
   uint32_t x = 0;

@@ -74,8 +74,8 @@ def requant_weights_oracle(orc, w, E, K, I):
 # [half][row][16 B], each 16 B = 4 words of 8 elements; bit b of element j's
 # E2M1 code (b = 0, 1, 2: magnitude m, e0, e1; b = 3: sign) sits at word bit
 # BIT_POS[j][b]; bytes [4096, ...) scale codes [row][64/gran].
-BIT_POS = [[6, 7, 8, 15], [22, 23, 24, 31], [3, 4, 5, 12], [19, 20, 21, 28],
-           [0, 1, 2, 9], [16, 17, 18, 25], [14, 10, 11, 13], [30, 26, 27, 29]]
+BIT_POS = [[14, 7, 8, 15], [30, 23, 24, 31], [0, 1, 2, 9], [16, 17, 18, 25],
+           [26, 27, 28, 3], [10, 11, 12, 19], [4, 5, 6, 13], [20, 21, 22, 29]]
 E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0.0, -.5, -1, -1.5, -2, -3, -4,
                  -6])
 
