@@ -377,3 +377,22 @@ def test_moe_edge_shapes(orc, E, K, I, T, k, record_property):
     y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
     check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=cfg.name,
                          record=record_property)
+
+
+@pytest.mark.parametrize("E,K,I,T,k", [
+    (4, 384, 384, 100, 2),    # FC1 and FC2 on the one-CTA block-scaled kernel
+    (3, 768, 256, 300, 3),    # FC1 on CTA pairs, FC2 (6 row blocks) on one CTA
+])
+def test_moe_fp8_edge_shapes(orc, E, K, I, T, k, record_property):
+    # Block counts that do not split over CTA pairs take the one-CTA
+    # block-scaled kernel.
+    cfg = synth.MoeConfig(f"fp8_edge_E{E}_K{K}_I{I}_T{T}_k{k}", E, K, I, T, k,
+                          act="fp8", weight_seed=5100 + E + K + I,
+                          input_seed=6100 + T)
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w, act=fp4.ACT_FP8)
+    assert p.desc.layout == 1
+    y, ws = gpu_forward(p, acts, cfg.top_k, fp4.ACT_FP8)
+    check_against_oracle(orc, cfg, w, acts, p, y, ws, range(T), what=cfg.name,
+                         record=record_property)
