@@ -377,24 +377,32 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const int sf = static_cast<int>(m % SF);
         const uint32_t phf = (m / SF) & 1u;
         if (!mbar_wait(fullF(sf), phf)) { ok = false; break; }
-        // Converts weight tile t of the stage: the 16 words of K columns
-        // 0..31 into va and those of 32..63 into vb.
-        auto convert = [&](int t, uint32_t (&va)[16], uint32_t (&vb)[16]) {
-          const uint8_t* f = smem + C::kFOff + sf * C::kFStage + t * a.tile_bytes;
-          const uint4 d0 = *reinterpret_cast<const uint4*>(f + r * 16);
-          const uint4 d1 = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
-          uint32_t s0, s1, s2, s3;    // bf16 scale pairs of the 16-wide groups
+        // Both tiles' packed words and scale pairs are read into registers
+        // first, so the F stage is released before the A-stage wait.
+        const uint8_t* f0 = smem + C::kFOff + sf * C::kFStage;
+        uint4 d[4];
+        uint32_t sc2[8];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint8_t* f = f0 + t * a.tile_bytes;
+          d[2 * t] = *reinterpret_cast<const uint4*>(f + r * 16);
+          d[2 * t + 1] = *reinterpret_cast<const uint4*>(f + 2048 + r * 16);
           if (a.gran == 16) {
             const uint8_t* sc = f + kTileDataBytes + r * 4;
-            s0 = sc[0] * smul2 + sadd2;
-            s1 = sc[1] * smul2 + sadd2;
-            s2 = sc[2] * smul2 + sadd2;
-            s3 = sc[3] * smul2 + sadd2;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc2[4 * t + j] = sc[j] * smul2 + sadd2;
           } else {
             const uint8_t* sc = f + kTileDataBytes + r * 2;
-            s0 = s1 = sc[0] * smul2 + sadd2;
-            s2 = s3 = sc[1] * smul2 + sadd2;
+            sc2[4 * t] = sc2[4 * t + 1] = sc[0] * smul2 + sadd2;
+            sc2[4 * t + 2] = sc2[4 * t + 3] = sc[1] * smul2 + sadd2;
           }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyF(sf));
+        auto convert = [&](int t, uint32_t (&va)[16], uint32_t (&vb)[16]) {
+          const uint4 d0 = d[2 * t], d1 = d[2 * t + 1];
+          const uint32_t s0 = sc2[4 * t], s1 = sc2[4 * t + 1], s2 = sc2[4 * t + 2],
+                         s3 = sc2[4 * t + 3];
           const uint4 w0 = dequant8(d0.x, s0), w1 = dequant8(d0.y, s0);
           const uint4 w2 = dequant8(d0.z, s1), w3 = dequant8(d0.w, s1);
           const uint4 w4 = dequant8(d1.x, s2), w5 = dequant8(d1.y, s2);
@@ -408,8 +416,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             vb[4 * x + 2] = wb[x].z; vb[4 * x + 3] = wb[x].w;
           }
         };
-        // The first tile is converted before waiting for the A stage, so
-        // the conversion overlaps the MMAs that still read the stage.
         uint32_t va[16], vb[16];
         convert(0, va, vb);
         if (!mbar_wait(emptyA(grp), pha ^ 1u)) { ok = false; break; }
@@ -419,8 +425,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         convert(1, va, vb);
         tmem_st16(t_st + 32u, va);
         tmem_st16(t_st + 48u, vb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(emptyF(sf));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
