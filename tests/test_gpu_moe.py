@@ -2,6 +2,8 @@
 against the FP64 oracle, within |gpu - oracle| <= 2^-7|oracle| + 1e-3 rms."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -297,6 +299,67 @@ def test_moe_deterministic_and_host_api(orc):
     fp4.moe_forward_host(xh, None, lh, p, cfg.top_k, yh, ws)
     torch.cuda.synchronize()
     assert torch.equal(yh.view(torch.int16), y1.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg", [synth.SMALL_DECODE, synth.SMALL_PREFILL, synth.SMALL_FP8],
+                         ids=lambda c: c.name)
+def test_moe_forward_graph_replay(cfg):
+    """moe_forward makes no host synchronisation or allocation after its
+    first call on a device, so it can be captured into a CUDA graph (how a
+    serving loop removes the per-call launch cost at a few tokens).  A
+    replay gives the eager call's bits, for the captured inputs and for new
+    inputs copied into the same buffers."""
+    w = weights_for(cfg)
+    act = fp4.ACT_FP8 if cfg.act == "fp8" else fp4.ACT_BF16
+    p = prepare(w, act=act)
+    k = cfg.top_k
+
+    def device_inputs(c):
+        acts = synth.moe_activations(c)
+        xb = bf16_tensor(acts["x_bf16"])
+        if act == fp4.ACT_FP8:
+            xq, xs = fp4.act_quant(xb)
+            return xq, xs, torch.from_numpy(acts["logits"]).cuda()
+        return xb, None, torch.from_numpy(acts["logits"]).cuda()
+
+    ws_bytes = max(fp4.moe_workspace_size(p, cfg.T, k), 256)
+
+    def eager(x, xs, lg):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        y = fp4.moe_forward(x, xs, lg, p, k, workspace=ws)
+        torch.cuda.synchronize()
+        return y
+
+    x0, xs0, lg0 = device_inputs(cfg)
+    other = dataclasses.replace(cfg, input_seed=cfg.input_seed + 17)
+    x1, xs1, lg1 = device_inputs(other)
+    y_ref0, y_ref1 = eager(x0, xs0, lg0), eager(x1, xs1, lg1)
+    # static buffers of the graph
+    xg, lgg = x0.clone(), lg0.clone()
+    xsg = xs0.clone() if xs0 is not None else None
+    yg = torch.empty_like(y_ref0)
+    wsg = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):       # warm-up call on the capture stream
+        fp4.moe_forward(xg, xsg, lgg, p, k, y=yg, workspace=wsg)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fp4.moe_forward(xg, xsg, lgg, p, k, y=yg, workspace=wsg)
+    yg.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == fp4.OK
+    assert torch.equal(yg.view(torch.int16), y_ref0.view(torch.int16))
+    xg.copy_(x1)
+    lgg.copy_(lg1)
+    if xsg is not None:
+        xsg.copy_(xs1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(yg.view(torch.int16), y_ref1.view(torch.int16))
 
 
 def test_moe_workspace_too_small():
