@@ -180,6 +180,31 @@ void stage_mark(int i, cudaStream_t st) {
   if (t_stage_on) cudaEventRecord(t_stage_ev[i], st);
 }
 
+// S2 + S3 without the gather: ids, w, counts, offsets, cstart (chunks of at
+// most `chunk` tokens), perm and inv.  Up to kTokPerBlk tokens take one
+// launch; more take route, scan and scatter (the same values).  Marks the
+// route and scan stages.
+cudaError_t route_permute(const float* logits, int T, int E, int k, int chunk, int32_t* hist,
+                          int32_t* base, int32_t* ids, float* w, int32_t* counts,
+                          int32_t* offsets, int32_t* cstart, int32_t* perm, int32_t* inv,
+                          int* err, cudaStream_t st) {
+  if (T <= kTokPerBlk) {
+    const cudaError_t e = launch_route_small(logits, T, E, k, chunk, ids, w, counts, offsets,
+                                             cstart, perm, inv, err, st);
+    stage_mark(1, st);
+    stage_mark(2, st);
+    return e;
+  }
+  cudaError_t e = launch_route(logits, T, E, k, ids, w, hist, err, st);
+  stage_mark(1, st);
+  if (e == cudaSuccess) e = launch_scan(T, E, hist, base, counts, offsets, cstart, chunk, st);
+  stage_mark(2, st);
+  if (e == cudaSuccess)
+    e = launch_scatter(ids, T, E, k, base, perm, inv, nullptr, nullptr, 0, FP4MOE_ACT_BF16,
+                       nullptr, err, st);
+  return e;
+}
+
 bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -219,14 +244,8 @@ int mx_forward(const fp4moe_packed* p, const MoeLayout& L, char* ws, const void*
     ~StageOff() { t_stage_on = false; }
   } stage_off;
   stage_mark(0, st);
-  cudaError_t e = launch_route(router_logits, T, p->E, top_k, ids, wts, hist, err, st);
-  stage_mark(1, st);
-  if (e == cudaSuccess)
-    e = launch_scan(T, p->E, hist, base, counts, offsets, cstart, kMxChunk, st);
-  stage_mark(2, st);
-  if (e == cudaSuccess)
-    e = launch_scatter(ids, T, p->E, top_k, base, perm, inv, nullptr, nullptr, 0,
-                       FP4MOE_ACT_FP8, nullptr, err, st);
+  cudaError_t e = route_permute(router_logits, T, p->E, top_k, kMxChunk, hist, base, ids, wts,
+                                counts, offsets, cstart, perm, inv, err, st);
   if (e == cudaSuccess)
     e = launch_gather_mx(inv, T, top_k, static_cast<const uint8_t*>(x), x_scales, p->K,
                          L.pitch, xperm, xs, err, st);
@@ -584,14 +603,10 @@ int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
     ~StageOff() { t_stage_on = false; }
   } stage_off;
   stage_mark(0, st);
-  cudaError_t e = launch_route(router_logits, T, p->E, top_k, ids, wts, hist, err, st);
-  stage_mark(1, st);
+  cudaError_t e = route_permute(router_logits, T, p->E, top_k, chunk, hist, base, ids, wts,
+                                counts, offsets, cstart, perm, inv, err, st);
   if (e == cudaSuccess)
-    e = launch_scan(T, p->E, hist, base, counts, offsets, cstart, chunk, st);
-  stage_mark(2, st);
-  if (e == cudaSuccess)
-    e = launch_scatter(ids, T, p->E, top_k, base, perm, inv, x, x_scales, p->K,
-                       p->act_mode, xperm, err, st);
+    e = launch_gather(inv, T, top_k, x, x_scales, p->K, p->act_mode, xperm, err, st);
   stage_mark(3, st);
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
 

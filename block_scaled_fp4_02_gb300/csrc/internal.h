@@ -52,6 +52,18 @@ cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
                            const void* x, const uint8_t* xs, int K,
                            int act_mode, uint16_t* xperm, int* err, cudaStream_t st);
 
+// S3 (gather alone): the activation rows in expert-major order, as above.
+cudaError_t launch_gather(const int32_t* inv, int T, int k, const void* x, const uint8_t* xs,
+                          int K, int act_mode, uint16_t* xperm, int* err, cudaStream_t st);
+
+// S2 + S3 (route, scan, scatter) for 1 <= T <= kTokPerBlk tokens in one
+// launch, with the outputs of launch_route + launch_scan + launch_scatter
+// (hist and base are not written).
+cudaError_t launch_route_small(const float* logits, int T, int E, int k, int chunk_max,
+                               int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                               int32_t* cstart, int32_t* perm, int32_t* inv, int* err,
+                               cudaStream_t st);
+
 // S7: y[t] = sum_j w[t,j] * o[inv[t,j]] -> bf16.
 cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
                            int T, int k, int K, uint16_t* y, int* err, cudaStream_t st);

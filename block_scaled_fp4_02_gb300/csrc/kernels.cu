@@ -237,6 +237,64 @@ __global__ void __launch_bounds__(256) h_fp8_round_kernel(
 // (larger value wins, equal values go to the lower expert id) select the
 // experts on the raw logits; w_j = exp(l_j - l_0) / sum over the k.
 
+// Top-k of token t by one warp: lane j < k receives the j-th expert and its
+// renormalised weight.
+template <int EPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E,
+                                            int k, int lane, int* err, int& my_id,
+                                            float& my_w) {
+  float v[EPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      v[i] = logits[static_cast<int64_t>(t) * E + e];
+      if (v[i] != v[i]) {
+        record_error(err, FP4MOE_ERR_INVALID_ARG);
+        v[i] = -INFINITY;
+      }
+    } else {
+      v[i] = -INFINITY;
+      taken |= 1u << i;
+    }
+  }
+  float my_v = 0.0f;
+  my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const int oi = __shfl_xor_sync(kFull, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_id = bi;
+    }
+  }
+  const float v0 = __shfl_sync(kFull, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - v0) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+  my_w = ex / sum;
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(1024) route_kernel(
     const float* __restrict__ logits, int T, int E, int k,
@@ -248,58 +306,12 @@ __global__ void __launch_bounds__(1024) route_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTokPerBlk + warp;
   if (t < T && warp < kTokPerBlk) {
-    float v[EPL];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        v[i] = logits[static_cast<int64_t>(t) * E + e];
-        if (v[i] != v[i]) {
-          record_error(err, FP4MOE_ERR_INVALID_ARG);
-          v[i] = -INFINITY;
-        }
-      } else {
-        v[i] = -INFINITY;
-        taken |= 1u << i;
-      }
-    }
-    float my_v = 0.0f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oi = __shfl_xor_sync(kFull, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_v = bv;
-        my_id = bi;
-      }
-    }
-    const float v0 = __shfl_sync(kFull, my_v, 0);
-    const float ex = (lane < k) ? expf(my_v - v0) : 0.0f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    int my_id;
+    float my_w;
+    route_token<EPL>(logits, t, E, k, lane, err, my_id, my_w);
     if (lane < k && in_bounds(err, my_id, E)) {
       ids[static_cast<int64_t>(t) * k + lane] = my_id;
-      w[static_cast<int64_t>(t) * k + lane] = ex / sum;
+      w[static_cast<int64_t>(t) * k + lane] = my_w;
       atomicAdd(&cnt[my_id], 1);
     }
   }
@@ -365,6 +377,71 @@ __global__ void __launch_bounds__(1024) scan_kernel(
   if (e == 0) {
     offsets[E] = total;
     cstart[E] = ctotal;
+  }
+}
+
+// Routing, scan and stable scatter of at most kTokPerBlk tokens in one
+// launch (the three kernels above and below do the same for any T, in
+// three): one warp per token as in route_kernel, the expert counts in
+// shared memory, the two block scans of scan_kernel, and the rank of pair p
+// among the pairs of its expert = the number of lower-indexed pairs of that
+// expert, so every output equals the three-kernel path's bit for bit.
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int chunk_max,
+    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ cstart,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int* err) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int pid[kTokPerBlk * kMaxTopK];   // expert of each pair, -1 if invalid
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < T) {
+    int my_id;
+    float my_w;
+    route_token<EPL>(logits, warp, E, k, lane, err, my_id, my_w);
+    if (lane < k) {
+      const bool ok = in_bounds(err, my_id, E);
+      pid[warp * k + lane] = ok ? my_id : -1;
+      if (ok) {
+        ids[warp * k + lane] = my_id;
+        w[warp * k + lane] = my_w;
+        atomicAdd(&cnt[my_id], 1);
+      }
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int tot = e < E ? cnt[e] : 0;
+  int total;
+  const int off = block_exclusive_scan(tot, &total);
+  const int nch = (e < E) ? (tot + chunk_max - 1) / chunk_max : 0;
+  int ctotal;
+  const int coff = block_exclusive_scan(nch, &ctotal);
+  if (e < E) {
+    counts[e] = tot;
+    offsets[e] = off;
+    cstart[e] = coff;
+  }
+  if (e == 0) {
+    offsets[E] = total;
+    cstart[E] = ctotal;
+  }
+  __syncthreads();                 // every count read before cnt becomes the base
+  if (e < E) cnt[e] = off;
+  __syncthreads();
+  const int P = T * k;
+  const int p = threadIdx.x;
+  if (p < P && pid[p] >= 0) {
+    const int ep = pid[p];
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (pid[q] == ep) ? 1 : 0;
+    const int pos = cnt[ep] + rank;
+    if (in_bounds(err, pos, P)) {
+      perm[pos] = p;
+      inv[p] = pos;
+    }
   }
 }
 
@@ -758,6 +835,25 @@ cudaError_t launch_route(const float* logits, int T, int E, int k,
   return cudaGetLastError();
 }
 
+cudaError_t launch_route_small(const float* logits, int T, int E, int k, int chunk_max,
+                               int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                               int32_t* cstart, int32_t* perm, int32_t* inv, int* err,
+                               cudaStream_t st) {
+  if (T < 1 || T > kTokPerBlk || k > kMaxTopK || E > kMaxE) return cudaErrorInvalidValue;
+  const int epl = (E + 31) / 32;
+#define FP4MOE_ROUTE_SMALL(N)                                                        \
+  route_small_kernel<N><<<1, 1024, 0, st>>>(logits, T, E, k, chunk_max, ids, w, counts, \
+                                            offsets, cstart, perm, inv, err)
+  if (epl <= 1) FP4MOE_ROUTE_SMALL(1);
+  else if (epl <= 2) FP4MOE_ROUTE_SMALL(2);
+  else if (epl <= 4) FP4MOE_ROUTE_SMALL(4);
+  else if (epl <= 8) FP4MOE_ROUTE_SMALL(8);
+  else if (epl <= 16) FP4MOE_ROUTE_SMALL(16);
+  else FP4MOE_ROUTE_SMALL(32);
+#undef FP4MOE_ROUTE_SMALL
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scan(int T, int E, const int32_t* hist, int32_t* base,
                         int32_t* counts, int32_t* offsets, int32_t* cstart,
                         int chunk_max, cudaStream_t st) {
@@ -783,7 +879,13 @@ cudaError_t launch_scatter(const int32_t* ids, int T, int E, int k,
   scatter_kernel<<<nblk, 512, smem, st>>>(ids, T, E, k, base, perm, inv, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || xperm == nullptr) return e;
+  return launch_gather(inv, T, k, x, xs, K, act_mode, xperm, err, st);
+}
+
+cudaError_t launch_gather(const int32_t* inv, int T, int k, const void* x, const uint8_t* xs,
+                          int K, int act_mode, uint16_t* xperm, int* err, cudaStream_t st) {
   const int64_t P = static_cast<int64_t>(T) * k;
+  if (P == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
   gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm, err);
   return cudaGetLastError();

@@ -362,6 +362,47 @@ def test_moe_forward_graph_replay(cfg):
     assert torch.equal(yg.view(torch.int16), y_ref1.view(torch.int16))
 
 
+@pytest.mark.parametrize("E,T,k,K,I,act", [
+    (8, 16, 2, 256, 256, fp4.ACT_BF16), (32, 13, 4, 256, 256, fp4.ACT_BF16),
+    (256, 1, 8, 256, 256, fp4.ACT_BF16), (256, 32, 8, 256, 256, fp4.ACT_BF16),
+    (64, 32, 16, 256, 256, fp4.ACT_BF16), (1024, 7, 8, 128, 128, fp4.ACT_BF16),
+    (32, 13, 4, 256, 256, fp4.ACT_FP8), (256, 32, 8, 256, 256, fp4.ACT_FP8)])
+def test_moe_few_tokens_routing_matches_three_kernels(E, T, k, K, I, act):
+    """Up to 32 tokens, moe_forward routes, scans and scatters in one launch;
+    its ids, weights, counts, offsets, perm and inv equal route_debug's
+    (route, scan and scatter as three kernels) bit for bit, with many tied
+    logits."""
+    cfg = synth.MoeConfig(f"few_tokens_E{E}_T{T}_k{k}", E, K, I, T, k,
+                          weight_seed=3201, input_seed=3301 + T)
+    p = prepare(weights_for(cfg), act=act)
+    acts = synth.moe_activations(cfg)
+    logits = (np.round(acts["logits"] * 4) / 4).astype(np.float32)
+    lg = torch.from_numpy(logits).cuda()
+    xb = bf16_tensor(acts["x_bf16"])
+    ws = torch.empty(max(fp4.moe_workspace_size(p, T, k), 256), dtype=torch.uint8,
+                     device="cuda")
+    if act == fp4.ACT_BF16:
+        fp4.moe_forward(xb, None, lg, p, k, workspace=ws)
+    else:
+        xq, xs = fp4.act_quant(xb)
+        fp4.moe_forward(xq, xs, lg, p, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == fp4.OK
+    ref = fp4.route_debug(lg, k)
+    offs = fp4.moe_workspace_offsets(p, T, k)
+    P = T * k
+
+    def region(name, n):
+        return ws[offs[name]:offs[name] + 4 * n].view(torch.int32)
+
+    assert torch.equal(region("ids", P), ref["ids"].view(-1))
+    assert torch.equal(region("w", P), ref["w"].view(-1).view(torch.int32))
+    assert torch.equal(region("counts", E), ref["counts"])
+    assert torch.equal(region("offsets", E + 1), ref["offsets"])
+    assert torch.equal(region("perm", P), ref["perm"])
+    assert torch.equal(region("inv", P), ref["inv"])
+
+
 def test_moe_workspace_too_small():
     cfg = synth.TINY
     p = prepare(weights_for(cfg))
