@@ -479,12 +479,14 @@ __global__ void __launch_bounds__(512) scatter_kernel(
 }
 
 // Activation gather: row p of the pair list goes to expert-major slot inv[p]
-// (one block per row, grid-stride over rows), as bf16; FP8 inputs are
+// (blocks (p, c) for c < gridDim.y share a row's 16-byte groups c,
+// c + gridDim.y, ...; grid-stride over rows), as bf16; FP8 inputs are
 // dequantized exactly on the way.
 __global__ void __launch_bounds__(256) gather_kernel(
     const int32_t* __restrict__ inv, int64_t P, int k, const void* __restrict__ x,
     const uint8_t* __restrict__ xs, int K, int act_mode, uint16_t* __restrict__ xperm,
     int* err) {
+  const int c0 = blockIdx.y * blockDim.x + threadIdx.x, cs = gridDim.y * blockDim.x;
   for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
     const int64_t t = p / k;
     const int64_t row = inv[p];
@@ -492,13 +494,13 @@ __global__ void __launch_bounds__(256) gather_kernel(
     uint4* dst = reinterpret_cast<uint4*>(xperm + row * K);
     if (act_mode == FP4MOE_ACT_BF16) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + t * K);
-      for (int c = threadIdx.x; c < K / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+      for (int c = c0; c < K / 8; c += cs) dst[c] = __ldg(src + c);
     } else {
       // FP8: bf16(e4m3 * 2^(xs - 127)), exact for scaled values in the
       // bf16 normal range.
       const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(x) + t * K);
       const uint8_t* srow = xs + t * (K / 32);
-      for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
+      for (int c = c0; c < K / 8; c += cs) {
         const uint2 q = src[c];
         const uint32_t sb = srow[c / 4];
         const float sc = (sb == 0)     ? __uint_as_float(0x00400000u)
@@ -531,7 +533,9 @@ __global__ void __launch_bounds__(256) combine_kernel(
       if (!in_bounds(err, pos[j], static_cast<int64_t>(gridDim.x) * k)) pos[j] = 0;
     }
   }
-  for (int n = threadIdx.x * 8; n < K; n += blockDim.x * 8) {
+  // Block (t, c) takes the 8-column groups c, c + gridDim.y, ... of token t.
+  const int stride = gridDim.y * blockDim.x * 8;
+  for (int n = (blockIdx.y * blockDim.x + threadIdx.x) * 8; n < K; n += stride) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -887,7 +891,12 @@ cudaError_t launch_gather(const int32_t* inv, int T, int k, const void* x, const
   const int64_t P = static_cast<int64_t>(T) * k;
   if (P == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>(P, static_cast<int64_t>(num_sms()) * 64));
-  gather_kernel<<<grid, 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm, err);
+  // Few rows: each row's 16-byte groups are split over several blocks, so
+  // that about two blocks per SM copy.
+  const int64_t groups = (K / 8 + 255) / 256;
+  const int split = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(groups, (2 * num_sms() + P - 1) / P)));
+  gather_kernel<<<dim3(grid, split), 256, 0, st>>>(inv, P, k, x, xs, K, act_mode, xperm, err);
   return cudaGetLastError();
 }
 
@@ -924,7 +933,12 @@ cudaError_t launch_gather_mx(const int32_t* inv, int T, int k, const uint8_t* x,
 cudaError_t launch_combine(const float* o, const int32_t* inv, const float* w,
                            int T, int k, int K, uint16_t* y, int* err, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 256, 0, st>>>(o, inv, w, k, K, y, err);
+  // A few tokens: each token's columns are split over several blocks, so
+  // that about two blocks per SM read the k rows (each output element is
+  // still summed by one thread in top-k order).
+  const int groups = (K + 2047) / 2048;
+  const int split = std::max(1, std::min(groups, (2 * num_sms() + T - 1) / T));
+  combine_kernel<<<dim3(T, split), 256, 0, st>>>(o, inv, w, k, K, y, err);
   return cudaGetLastError();
 }
 
