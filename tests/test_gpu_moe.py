@@ -403,6 +403,42 @@ def test_moe_few_tokens_routing_matches_three_kernels(E, T, k, K, I, act):
     assert torch.equal(region("inv", P), ref["inv"])
 
 
+def test_moe_host_api_two_streams():
+    """Calls on two streams at once, each with its own workspace and output
+    buffer (how the end-to-end measurement overlaps one step's copies with
+    the other's kernels), give the one-stream bits: the forward keeps no
+    device state between calls but the status word."""
+    cfg = synth.SMALL_PREFILL
+    w = weights_for(cfg)
+    acts = synth.moe_activations(cfg)
+    p = prepare(w)
+    y_ref, _ = gpu_forward(p, acts, cfg.top_k, fp4.ACT_BF16)
+    other = dataclasses.replace(cfg, input_seed=cfg.input_seed + 5)
+    acts2 = synth.moe_activations(other)
+    y_ref2, _ = gpu_forward(p, acts2, cfg.top_k, fp4.ACT_BF16)
+
+    def host(a):
+        xh = torch.from_numpy(a["x_bf16"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        return xh, torch.from_numpy(a["logits"]).pin_memory()
+
+    ins = [host(acts), host(acts2)]
+    refs = [y_ref.cpu(), y_ref2.cpu()]
+    n = fp4.moe_workspace_size_host(p, cfg.T, cfg.top_k)
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    wss = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = [[torch.empty(cfg.T, cfg.K, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+            for _ in range(2)]
+    for i in range(3):
+        for j in range(2):
+            fp4.moe_forward_host(ins[j][0], None, ins[j][1], p, cfg.top_k, outs[j][i],
+                                 wss[j], stream=streams[j])
+    torch.cuda.synchronize()
+    assert fp4.last_device_error() == fp4.OK
+    for j in range(2):
+        for i in range(3):
+            assert torch.equal(outs[j][i].view(torch.int16), refs[j].view(torch.int16))
+
+
 def test_moe_workspace_too_small():
     cfg = synth.TINY
     p = prepare(weights_for(cfg))
