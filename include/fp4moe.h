@@ -200,7 +200,11 @@ size_t fp4moe_moe_workspace_size(const fp4moe_packed* p, int T, int top_k);
  *   workspace     >= fp4moe_moe_workspace_size(p, T, top_k) bytes, 256-byte
  *                 aligned; contents are scratch.
  * T >= 0 (T == 0 is a no-op), 1 <= top_k <= min(E, 16).  The mode is the
- * act_mode the weights were prepared for. */
+ * act_mode the weights were prepared for.  Asynchronous: no host
+ * synchronisation, and after the first call on a device (which sets the
+ * kernels' per-device attributes) no allocation either, so the call may be
+ * captured into a CUDA graph.  Calls that can run at once (other streams)
+ * need their own workspace and y; the status word is shared. */
 int fp4moe_moe_forward(const void* x, const uint8_t* x_scales,
                        const float* router_logits, int T,
                        const fp4moe_packed* p, int top_k, void* y,
