@@ -120,7 +120,13 @@ struct Cfg {
   // cstart[0..E] and offsets[0..E] copied to shared memory for the per-unit
   // lookups of every role.
   static constexpr uint32_t kTabOff = kBarOff + 8 * kNumBars + 16;
-  static constexpr uint32_t kSmem = kTabOff + 8 * (kMaxE + 1) + 1024;
+  // TMEM A: the CTA's work units (expert, block, first row, tokens), decoded
+  // once at the start for up to kUnitTab units: every role then reads a
+  // unit instead of searching the expert table at each unit boundary, where
+  // the search sat on the MMA and activation producers' hand-off chain.
+  static constexpr int kUnitTab = kATmem ? 640 : 0;
+  static constexpr uint32_t kUnitOff = (kTabOff + 8 * (kMaxE + 1) + 15) & ~15u;
+  static constexpr uint32_t kSmem = kUnitOff + 16 * kUnitTab + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kATmem ? (kAccBufs * kAccCols <= kATmemCol &&
                           kATmemCol + 64 * kSAa <= kTmemCols)
@@ -201,6 +207,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = nbu * tab_cs[a.E];
+  const int nloc = static_cast<int>(blockIdx.x) < total
+                       ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                       : 0;
+  const bool utab = nloc <= C::kUnitTab;   // uniform over the block
+  int4* utab_s = reinterpret_cast<int4*>(smem + C::kUnitOff);
+  if (utab) {
+    for (int i = threadIdx.x; i < nloc; i += blockDim.x) {
+      const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, blockIdx.x + i * gridDim.x);
+      utab_s[i] = make_int4(U.e, U.nb, U.row0, U.ntok);
+    }
+    __syncthreads();
+  }
+  // Unit u, the iu-th of this CTA.
+  auto unit_at = [&](int iu, int u) -> Unit {
+    if (utab) {
+      const int4 v = utab_s[iu];
+      return Unit{v.x, v.y, v.z, v.w};
+    }
+    return decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
+  };
 
   if (warp == kWarpFProd) {
     // ------------------------------------------------- weight producer
@@ -208,8 +234,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       int s = 0;
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
+      for (int u = blockIdx.x, iu = 0; u < total && ok; u += gridDim.x, ++iu) {
+        const Unit U = unit_at(iu, u);
         const int tiles = min(MT, a.nblocks - U.nb);
         const uint8_t* wt = a.wpack + (static_cast<int64_t>(U.e) * a.nblocks + U.nb) *
                                           a.ksteps * a.tile_bytes;
@@ -247,8 +273,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       const int bp = (warp == kWarpBProd) ? 0 : (warp == kWarpMma) ? 1 : 2 + (warp - C::kWarpBX0);
       uint32_t n = 0, issued = 0, issued_ph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
+      for (int u = blockIdx.x, iu = 0; u < total && ok; u += gridDim.x, ++iu) {
+        const Unit U = unit_at(iu, u);
         const int nbox = (U.ntok + C::kBoxRows - 1) / C::kBoxRows;
         constexpr uint32_t kBoxBytes = C::kBoxRows * 128u;
         for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
@@ -295,8 +321,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       bool ok = true;
       const uint64_t adesc0 = sw128_kmajor_desc(sbase + C::kAOff);
       const uint64_t bdesc0 = sw128_kmajor_desc(sbase + C::kBOff);
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
+      for (int u = blockIdx.x, iu = 0; u < total && ok; u += gridDim.x, ++iu) {
+        const Unit U = unit_at(iu, u);
         const int tiles = min(MT, a.nblocks - U.nb);
         const uint32_t nn = static_cast<uint32_t>((U.ntok + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, nn);
@@ -450,8 +476,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int tile = grp;
     uint32_t n = 0;                   // global K-step counter of this CTA
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const bool live = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u).nb + tile < a.nblocks;
+    for (int u = blockIdx.x, iu = 0; u < total && ok; u += gridDim.x, ++iu) {
+      const bool live = unit_at(iu, u).nb + tile < a.nblocks;
       for (int ks = 0; ks < a.ksteps; ++ks, ++n) {
         const int sf = static_cast<int>(n % SF), sa = static_cast<int>(n % SAa);
         const uint32_t phf = (n / SF) & 1u, pha = (n / SAa) & 1u;
@@ -515,8 +541,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     uint32_t acc_ph = 0;
     uint32_t n_unit = 0;              // K steps of this CTA before the unit
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, n_unit += a.ksteps) {
-      const Unit U = decode_unit(a, nbu, MT, NT, tab_cs, tab_os, u);
+    for (int u = blockIdx.x, iu = 0; u < total && ok;
+         u += gridDim.x, ++iu, n_unit += a.ksteps) {
+      const Unit U = unit_at(iu, u);
       if (!mbar_wait(accFull(buf), acc_ph)) { ok = false; break; }
       tc_fence_after();
       const float alpha = __ldg(a.alpha + U.e);
