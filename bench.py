@@ -390,19 +390,22 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_moe_gemm_fc1.json")
 
 def measured_traffic(workload: str):
     """FC1 DRAM bytes per launch from the committed ncu capture (scaled
-    from a small case, see the file), or None when the GEMM sources have
-    changed since the capture or no capture covers this workload."""
+    from a small case, see the file), or None when the sources of that
+    workload's FC1 kernel have changed since the capture or no capture
+    covers this workload."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
+        entry = t["per_launch_bytes"].get(workload)
+        if entry is None:
+            return None
         h = hashlib.sha256()
-        for rel in t["source_files"]:
+        for rel in entry["source_files"]:
             with open(os.path.join(ROOT, rel), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest() != t["source_sha256"]:
+        if h.hexdigest() != entry["source_sha256"]:
             return None
-        entry = t["per_launch_bytes"].get(workload)
-        return None if entry is None else float(entry["bytes"])
+        return float(entry["bytes"])
     except (OSError, KeyError, ValueError):
         return None
 
