@@ -228,10 +228,13 @@ class MoeRun:
         between two kernels costs the stream ~2-3 us, so a shorter step is
         timed again as a whole, without them, for its value."""
         torch, fp4 = self.torch, self.fp4
-        th = time.perf_counter()
+        host = []
         for _ in range(warmup):
+            th = time.perf_counter()
             self.step()
-        host_step = (time.perf_counter() - th) / max(warmup, 1)
+            host.append(time.perf_counter() - th)
+        # the host's enqueue time of a step, first (module loading) call aside
+        host_step = float(np.median(host[1:] if len(host) > 1 else host or [0.0]))
         torch.cuda.synchronize()
         ev = torch.cuda.Event
         stage = [[ev(enable_timing=True) for _ in range(fp4.STAGE_EVENTS)]
@@ -289,10 +292,12 @@ class MoeRun:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step()
-        th = time.perf_counter()
+        host = []
         for _ in range(max(warmup, 1)):
+            th = time.perf_counter()
             g.replay()
-        host_step = (time.perf_counter() - th) / max(warmup, 1)
+            host.append(time.perf_counter() - th)
+        host_step = float(np.median(host))
         torch.cuda.synchronize()
         t0, t1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
         torch.cuda._sleep(int((1.5 * steps * host_step + 5e-4) * 2.2e9))
