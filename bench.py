@@ -247,10 +247,11 @@ class MoeRun:
 
         # A small step's launches can take the host longer to enqueue than
         # the device to run (T <= 16 tokens): the timed steps queue behind a
-        # device-side delay that outlasts their enqueueing, so the events
-        # measure device time.
+        # device-side delay that outlasts their enqueueing (with stage events
+        # a step takes the host longer than in the warm-up: a factor of 3),
+        # so the events measure device time.
         def delay():
-            torch.cuda._sleep(int((1.5 * steps * host_step + 5e-4) * 2.2e9))
+            torch.cuda._sleep(int((3.0 * steps * host_step + 2e-3) * 2.2e9))
 
         def run(with_stages):
             delay()
