@@ -626,7 +626,8 @@ def main():
             ms = float(t.item())
         e2e = {"value": cfg.T * args.steps * world / (ms / 1e3),
                "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+               "streams": 2}
 
     extra = {}
     names = [] if args.extra == "none" else [
@@ -689,7 +690,10 @@ def main():
                    "I": cfg.I, "top_k": cfg.top_k, "weights": "NVFP4 g16",
                    "activations": cfg.act, "parallelism": "replicas",
                    "l2": "inputs larger than L2 (packed weights "
-                         f"{(run.packed.desc.w13_bytes + run.packed.desc.w2_bytes) / 1e9:.2f} GB)"},
+                         f"{(run.packed.desc.w13_bytes + run.packed.desc.w2_bytes) / 1e9:.2f} GB)",
+                   "timing": "CUDA events on the launching stream, steps queued behind a "
+                             "device-side delay; stage times from events between the stages "
+                             "(a step under 2 ms valued by a second pass without them)"},
         "tflops": head["tflops"] * world, "weight_gbs": head["weight_gbs"],
         "layer_hbm_frac": head["layer_hbm_frac"],
         "layer_tensor_frac": head.get("layer_tensor_frac"),
