@@ -261,8 +261,9 @@ int fp4moe_route_debug(const float* logits, int T, int E, int top_k,
  * stage boundaries: [0] start, [1] after routing, [2] after the scan,
  * [3] after the scatter/gather, [4] after FC1, [5] after the FP8 rounding of
  * h (same point as [4] in BF16 mode), [6] after FC2, [7] after the combine;
- * then the hand-over is cleared.  events == NULL clears it.  INVALID_ARG if
- * n is wrong. */
+ * then the hand-over is cleared.  Up to 32 tokens, routing, scan and scatter
+ * are one launch, which [1] and [2] both follow.  events == NULL clears it.
+ * INVALID_ARG if n is wrong. */
 #define FP4MOE_STAGE_EVENTS 8
 int fp4moe_set_stage_events(void* const* events, int n);
 
